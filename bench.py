@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark of the GroupQueryAttention hot path over a shared KV buffer.
+
+Headline: batched decode (16 sequences, 32 query / 8 KV heads, head size
+128, bf16, buffer of 4096 slots, past lengths uniform in [1, 4095], one new
+token each).  One step = one gqa_forward call: rotary embedding of the new
+query/key rows, scatter-append of the new K/V rows, split-KV attention over
+each sequence's true length, split combine.  The metric is algorithmic KV
+bytes per second (visible K and V rows, plus query, output and the appended
+rows) over the whole step.
+
+The other workloads (long-context decode with and without a 4096 window,
+the 2048-token prefill and the chunked prefill with bias) are timed after it
+and reported under "also".
+
+--impl reference times the CPU oracle (the plain reference implementation
+of the same operator) on the host cores, on a bounded sample of the same
+workload.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload; there
+is no data exchange between ranks (replicas only, weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "decode_b16"
+METRIC = "GQA decode KV GB/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_init(backend):
+    import torch.distributed as dist
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return int(os.environ.get("RANK", "0")), ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws, device=None):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the GPU works
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.samples if t0 <= t <= t1 and len(r) >= 9]
+        if not rows:
+            rows = [r for (_, r) in self.samples if len(r) >= 9]
+        if not rows:
+            return {"error": "no nvidia-smi samples"}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def gpu_selector(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(dev)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Problem:
+    """Device-resident inputs of one workload, with `sets` copies of the
+    buffers that consecutive steps rotate through (so a step never finds the
+    previous step's KV rows in L2 when one set is smaller than L2)."""
+
+    def __init__(self, name, device, sets=1):
+        import torch
+        import shared_kv_cache_gb300 as gqa
+        from shared_kv_cache_gb300 import workloads as W
+        self.w = W.CONFIGS[name]
+        inp = W.make_inputs(self.w, device=device, sentinel=False)
+        self.inp = inp
+        self.past = inp["seqlens_k"].cpu()
+        w = self.w
+        self.dims = gqa.make_dims(w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len,
+                                  w.dtype, 0, inp["cos"].shape[0] if inp["cos"] is not None else 0,
+                                  *(inp["attention_bias"].shape[:2] if inp["attention_bias"] is not None else (1, 1)))
+        self.total = inp["total_sequence_length"]
+        self.ws_bytes = gqa.gqa_workspace_size(self.dims, self.total, w.local_window_size)
+        self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
+        self.kbufs = [inp["k_buf"]] + [inp["k_buf"].clone() for _ in range(sets - 1)]
+        self.vbufs = [inp["v_buf"]] + [inp["v_buf"].clone() for _ in range(sets - 1)]
+        self.out = torch.empty_like(inp["query"])
+        self.decode = w.seq_len == 1
+        self.bytes = W.decode_bytes(w, self.past)
+        self.flops = W.prefill_flops(w, self.past) if not self.decode else 0
+        self.gqa = gqa
+
+    def step(self, i, stream):
+        d = self.inp
+        r = i % len(self.kbufs)
+        st = self.gqa.gqa_forward(self.dims, d["query"], d["key"], d["value"], self.kbufs[r], self.vbufs[r],
+                                  self.kbufs[r], self.vbufs[r], d["seqlens_k"], self.total, d["cos"], d["sin"],
+                                  d["scale"], d["local_window_size"], d["attention_bias"], self.out, self.ws,
+                                  self.ws.numel(), stream)
+        if st != 0:
+            raise RuntimeError(self.gqa.gqa_status_string(st))
+
+    def launches_per_step(self):
+        # decode: the split-KV kernel, plus the combine kernel when a sequence spans splits;
+        # prefill: rotary/append kernel plus the attention kernel
+        if self.decode:
+            return 2 if self.ws_bytes > 0 else 1
+        return 2
+
+
+def time_steps(prob, steps, warmup, stream, ws_count=1, device=None):
+    import torch
+    for i in range(warmup):
+        prob.step(i, stream)
+    torch.cuda.synchronize()
+    barrier(ws_count)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(steps):
+        prob.step(i, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(ws_count)
+    ms = e0.elapsed_time(e1) / steps
+    return max_over_ranks(ms, ws_count, device), t0, t1
+
+
+def e2e_decode(prob, steps, warmup, stream):
+    """Through the tensor-level API with host buffers: every step copies the
+    new query/key/value rows and seqlens_k from pinned host memory, runs the
+    step and copies the output back."""
+    import torch
+    import shared_kv_cache_gb300 as gqa
+    d = prob.inp
+    hq, hk, hv = (d[n].cpu().pin_memory() for n in ("query", "key", "value"))
+    hs = d["seqlens_k"].cpu().pin_memory()
+    hout = torch.empty(prob.out.shape, dtype=prob.out.dtype).pin_memory()
+    dq, dk, dv, ds = (torch.empty_like(d[n]) for n in ("query", "key", "value", "seqlens_k"))
+    wsp = gqa.Workspace()
+    w = prob.w
+
+    def one(i):
+        r = i % len(prob.kbufs)
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        ds.copy_(hs, non_blocking=True)
+        out = gqa.forward(dq, dk, dv, prob.kbufs[r], prob.vbufs[r], ds, prob.total, w.num_heads, w.kv_num_heads,
+                          d["cos"], d["sin"], d["scale"], d["local_window_size"], d["attention_bias"],
+                          output=prob.out, workspace=wsp, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            one(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            one(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs))
+    d2h = hout.numel() * hout.element_size()
+    return ms, h2d, d2h
+
+
+def cpu_baseline(name, min_seconds=10.0, batches=None):
+    """Times the CPU oracle in a fresh interpreter (spawned, so no CUDA state
+    is inherited) with every host core available to numpy."""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import oracle
+from shared_kv_cache_gb300 import workloads as W
+w = W.CONFIGS[{name!r}]
+inp = W.make_inputs(w, sentinel=False)
+batches = {batches!r}
+args = (W.bits(inp["query"]), W.bits(inp["key"]), W.bits(inp["value"]), W.bits(inp["k_buf"]), W.bits(inp["v_buf"]),
+        inp["seqlens_k"].numpy(), inp["total_sequence_length"], W.bits(inp["cos"]), W.bits(inp["sin"]),
+        w.num_heads, w.kv_num_heads, inp["scale"], inp["local_window_size"], None, w.dtype)
+import torch
+past = inp["seqlens_k"]
+sel = list(range(w.batch)) if batches is None else batches
+nbytes = W.decode_bytes(w.with_(batch=len(sel)), past[sel])
+n, t0 = 0, time.perf_counter()
+while True:
+    st = oracle.gqa_forward(*args, batches=sel)[0]
+    assert st == 0
+    n += 1
+    if time.perf_counter() - t0 >= {min_seconds!r}:
+        break
+dt = time.perf_counter() - t0
+print(json.dumps({{"value": nbytes * n / dt / 1e9, "calls": n, "seconds": dt, "sequences": len(sel)}}))
+"""
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": res["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{res['sequences']} of the batch's sequences per call, {res['calls']} calls in "
+                      f"{res['seconds']:.1f} s (numpy float64, {cores} host threads available)"}
+
+
+def run_ours(args):
+    import torch
+    rank, ws = dist_init("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    import shared_kv_cache_gb300 as gqa
+    gqa.load_library()
+    pk = peaks()
+    stream = torch.cuda.Stream(device)
+
+    # headline: batched decode, rotating four buffer sets (4 x 268 MB > L2)
+    prob = Problem(HEADLINE, device, sets=4)
+    sampler = ClockSampler(gpu_selector(torch, local))
+    sampler.start()
+    # keep the GPU busy for ~1 s before timing so that the clock record reflects load
+    tb = time.time()
+    i = 0
+    while time.time() - tb < 1.0:
+        prob.step(i, stream)
+        i += 1
+        if i % 200 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    ms, t0, t1 = time_steps(prob, args.steps, max(args.warmup, 3), stream, ws, device)
+    sampler.stop()
+    clocks = sampler.summary(tb, t1)
+    gbs = prob.bytes / (ms * 1e-3) / 1e9
+    value = gbs * ws
+
+    e2e_ms, h2d, d2h = e2e_decode(prob, args.steps, max(args.warmup, 3), stream)
+    e2e = {"value": prob.bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    roofline = {"kernel": "decode_kernel + combine_kernel (one gqa_forward call)", "bound": "hbm",
+                "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                "peak_source": pk["source"], "frac_of_nominal_8tbs": gbs / 8000.0,
+                "bytes_per_launch": prob.bytes, "traffic": None}
+
+    also = []
+    if not args.no_also:
+        for name, sets in (("long_decode", 1), ("long_decode_w4096", 4), ("prefill_2k", 1),
+                           ("chunked_prefill", 4)):
+            p = Problem(name, device, sets=sets)
+            steps = 20 if not p.decode else 50
+            m, _, _ = time_steps(p, steps, 3, stream, ws, device)
+            if p.decode:
+                v = p.bytes / (m * 1e-3) / 1e9
+                also.append({"workload": name, "metric": "GQA decode KV GB/s", "value": v, "unit": "GB/s",
+                             "ms_per_step": m, "frac": v / pk["hbm_gbs"], "peak": pk["hbm_gbs"]})
+            else:
+                v = p.flops / (m * 1e-3) / 1e12
+                also.append({"workload": name, "metric": "GQA prefill attention TFLOP/s", "value": v,
+                             "unit": "TFLOP/s", "ms_per_step": m, "frac": v / pk["bf16_tflops"],
+                             "peak": pk["bf16_tflops"], "kv_gbs": p.bytes / (m * 1e-3) / 1e9})
+            del p
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = cpu_baseline(HEADLINE)
+
+    w = prob.w
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V and cache)",
+        "config": {"workload": HEADLINE, "batch": w.batch, "num_heads": w.num_heads,
+                   "kv_num_heads": w.kv_num_heads, "head_size": w.head_size, "max_seq_len": w.max_seq_len,
+                   "new_tokens": w.seq_len, "past_lengths": f"uniform [{w.past_lo}, {w.past_hi}]",
+                   "rotary": True, "bytes_per_step": prob.bytes,
+                   "l2": "4 rotating KV buffer sets (4 x 268 MB) > 129 MB L2",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": prob.launches_per_step() * args.steps,
+        "clocks": clocks, "also": also,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    import oracle
+    from shared_kv_cache_gb300 import workloads as W
+    w = W.CONFIGS[HEADLINE]
+    inp = W.make_inputs(w, sentinel=False)
+    sel = [0, 1]   # a bounded sample: two of the sixteen sequences per step
+    a = (W.bits(inp["query"]), W.bits(inp["key"]), W.bits(inp["value"]), W.bits(inp["k_buf"]),
+         W.bits(inp["v_buf"]), inp["seqlens_k"].numpy(), inp["total_sequence_length"], W.bits(inp["cos"]),
+         W.bits(inp["sin"]), w.num_heads, w.kv_num_heads, inp["scale"], 0, None, w.dtype)
+    nbytes = W.decode_bytes(w.with_(batch=len(sel)), inp["seqlens_k"][sel])
+    for _ in range(max(args.warmup, 3)):
+        oracle.gqa_forward(*a, batches=sel)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gqa_forward(*a, batches=sel)
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    value = nbytes / (ms * 1e-3) / 1e9
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": HEADLINE, "batch": w.batch, "num_heads": w.num_heads,
+                   "kv_num_heads": w.kv_num_heads, "head_size": w.head_size, "max_seq_len": w.max_seq_len},
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "GB/s",
+                         "sample": f"sequences {sel} of the {w.batch}-sequence batch per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

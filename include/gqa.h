@@ -1,0 +1,146 @@
+/*
+ * gqa.h -- C ABI of libgqa: GroupQueryAttention over a shared, pre-allocated
+ * BNSH key/value buffer, for one NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes (sources: the onnxruntime discussion "Clarification
+ * about GroupQueryAttention behavior" -- the quoted past_key text and
+ * tianleiwu's reply; the torch-mlir PR "[TorchOnnxToTorch] Add pad+scatter KV
+ * cache and mask to GQA" -- its description; the rocMLIR discussion "KV
+ * Cache" -- "Example" and "Short summary of notes"):
+ *
+ *   for every sequence b with past length P_b = seqlens_k[b] and every new
+ *   token i < S, at position p = P_b + i:
+ *   (1) rotary embedding of the new query and key rows at position p
+ *       (position ids = arange plus the past length);
+ *   (2) the rotated key row and the value row are written into the shared
+ *       buffer at slot p of every KV head (scatter-append at seqlens_k);
+ *   (3) query head h attends over KV head h / (H / Hkv), over keys
+ *       j <= p (causal) and, when local_window_size W > 0, j > p - W; the
+ *       scan stops at the sequence's true length P_b + S, never at
+ *       max_seq_len; an optional additive attention_bias is added to the
+ *       scaled scores;
+ *   (4) when the buffer has no room for the new tokens the call fails with
+ *       GQA_ERR_KV_OVERFLOW and writes nothing.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device pointers on the current
+ *     device; "host" pointers are ordinary host memory.  All device pointers
+ *     must be 16-byte aligned.
+ *   - The caller owns every buffer.  The library allocates no device memory
+ *     per call; it keeps one small error word per device in a static device
+ *     variable.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Argument errors and overflow that the host can see
+ *     are reported before anything is launched, so no buffer is touched.
+ *     Errors only the device can see (a seqlens_k entry beyond the buffer, a
+ *     bounded wait inside a kernel that ran out) are recorded in the device
+ *     error word; the kernels skip the affected writes and never trap.
+ *     gqa_check_device_status() reports and clears that word.
+ *   - No function throws across the ABI.
+ */
+#ifndef GQA_H_
+#define GQA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GQA_OK = 0,
+  GQA_ERR_INVALID_ARGUMENT = 1, /* bad dims, null or misaligned pointer, small workspace */
+  GQA_ERR_KV_OVERFLOW = 2,      /* the shared buffer has no room for the new tokens */
+  GQA_ERR_UNSUPPORTED = 3,      /* a valid operator form this library does not implement */
+  GQA_ERR_CUDA = 4,             /* a CUDA runtime call failed */
+  GQA_ERR_TIMEOUT = 5           /* a bounded wait inside a kernel ran out */
+} gqa_status_t;
+
+typedef enum { GQA_DTYPE_FP16 = 0, GQA_DTYPE_BF16 = 1 } gqa_dtype_t;
+
+/* Problem dimensions.  All are runtime values. */
+typedef struct {
+  int32_t batch;              /* B >= 1 */
+  int32_t seq_len;            /* S >= 1: new tokens per sequence (1 = decode) */
+  int32_t num_heads;          /* H: query heads */
+  int32_t kv_num_heads;       /* Hkv: key/value heads; H % Hkv == 0 */
+  int32_t head_size;          /* D: multiple of 8, at most 256 */
+  int32_t max_seq_len;        /* M: slots per (sequence, KV head) in the shared buffer */
+  int32_t dtype;              /* gqa_dtype_t: element type T of every T array */
+  int32_t rotary_interleaved; /* 0: dimension j pairs with j + D/2; 1: j pairs with j + 1 (2j, 2j+1) */
+  int32_t cos_cache_rows;     /* rows of cos/sin caches; ignored when cos_cache is NULL */
+  int32_t bias_batch;         /* 1 or B; ignored when attention_bias is NULL */
+  int32_t bias_heads;         /* 1 or H; ignored when attention_bias is NULL */
+} gqa_dims_t;
+
+/*
+ * gqa_forward -- one GroupQueryAttention step over the shared buffer.
+ *
+ *   dims             host: problem dimensions (above).
+ *   query            device, T [B, S, H*D]   new query rows (heads contiguous per token).
+ *   key, value       device, T [B, S, Hkv*D] new key/value rows.
+ *   past_key         device, T [B, Hkv, M, D] the shared buffer.  It must be the same
+ *   present_key      pointer as present_key (and past_value as present_value): the
+ *   past_value       operator's shared past/present binding.  Different pointers
+ *   present_value    return GQA_ERR_UNSUPPORTED.  Only slots [P_b, P_b + S) of each
+ *                    (b, KV head) are written; every other slot keeps its bits.
+ *   seqlens_k        device, int32 [B]: past length P_b of each sequence (0 = empty).
+ *   total_sequence_length  host scalar: an upper bound on P_b + S for every b and the
+ *                    last dimension of attention_bias.  Must be >= S.  Larger than M:
+ *                    GQA_ERR_KV_OVERFLOW before any launch.  A sequence with
+ *                    P_b + S > M (or P_b < 0, or P_b + S > total_sequence_length) is
+ *                    detected on the device: that sequence is skipped entirely (no
+ *                    slot, no output row written) and the device error word records
+ *                    GQA_ERR_KV_OVERFLOW (resp. GQA_ERR_INVALID_ARGUMENT).
+ *   cos_cache,       device, T [cos_cache_rows, D/2]: cos/sin of the rotary angle of
+ *   sin_cache        position p and pair j.  Both NULL: no rotary embedding.
+ *                    cos_cache_rows must be >= total_sequence_length.
+ *   scale            score scale; <= 0 means 1/sqrt(D).
+ *   local_window_size  <= 0: full causal attention; W > 0: each token sees the W most
+ *                    recent positions up to and including its own.
+ *   attention_bias   device, T [bias_batch, bias_heads, S, total_sequence_length] or
+ *                    NULL; indexed by absolute key position.
+ *   output           device, T [B, S, H*D].
+ *   workspace        device scratch of at least gqa_workspace_size() bytes (may be NULL
+ *                    when that size is 0).  Its contents on entry do not matter.
+ *   stream           cudaStream_t.
+ *
+ * Returns GQA_OK once the work is enqueued.
+ */
+gqa_status_t gqa_forward(const gqa_dims_t* dims,
+                         const void* query, const void* key, const void* value,
+                         const void* past_key, const void* past_value,
+                         void* present_key, void* present_value,
+                         const int32_t* seqlens_k, int32_t total_sequence_length,
+                         const void* cos_cache, const void* sin_cache,
+                         float scale, int32_t local_window_size,
+                         const void* attention_bias,
+                         void* output,
+                         void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
+ * gqa_workspace_size -- bytes of device scratch gqa_forward needs for these
+ * dims, total_sequence_length and local_window_size (rotated queries for the
+ * prefill kernels, per-split partial results for split-KV decode).  The
+ * figure is for the current device and covers calls with or without rotary
+ * embedding.  Returns 0 for invalid dims (and when no scratch is needed).
+ */
+size_t gqa_workspace_size(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size);
+
+/*
+ * gqa_check_device_status -- synchronise `stream`, then report and clear the
+ * current device's error word (GQA_OK when no kernel recorded an error), or
+ * GQA_ERR_CUDA when a CUDA call or an earlier launch failed.
+ */
+gqa_status_t gqa_check_device_status(void* stream);
+
+/* gqa_status_string -- a static, human-readable name for a status code. */
+const char* gqa_status_string(gqa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H_ */

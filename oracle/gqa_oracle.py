@@ -84,26 +84,36 @@ def positions(seqlens_k: np.ndarray, seq_len: int) -> np.ndarray:
 
 
 def rotary(x_bits: np.ndarray, pos: np.ndarray, cos_bits: np.ndarray, sin_bits: np.ndarray,
-           dtype: str) -> np.ndarray:
-    """Non-interleaved rotary embedding of x [B, S, heads, D] at positions
-    pos [B, S]: dimension j is paired with j + D/2 and rotated by the angle
+           dtype: str, interleaved: bool = False) -> np.ndarray:
+    """Rotary embedding of x [B, S, heads, D] at positions pos [B, S].  Pair j
+    (j < D/2) is (x[j], x[j + D/2]) in the non-interleaved layout and
+    (x[2j], x[2j + 1]) in the interleaved one; it is rotated by the angle
     whose cosine and sine are cos/sin[pos, j]:
-        y[j]       = x[j] * c - x[j + D/2] * s
-        y[j + D/2] = x[j + D/2] * c + x[j] * s
+        y1 = x1 * c - x2 * s
+        y2 = x2 * c + x1 * s
     in fp32, products first, no fused multiply-add, then rounded to T."""
     D = x_bits.shape[-1]
     half = D // 2
     x = t_to_f32(x_bits, dtype)
     c = t_to_f32(cos_bits, dtype)[pos][:, :, None, :]   # [B, S, 1, D/2]
     s = t_to_f32(sin_bits, dtype)[pos][:, :, None, :]
-    x1 = x[..., :half]
-    x2 = x[..., half:]
+    if interleaved:
+        x1 = x[..., 0::2]
+        x2 = x[..., 1::2]
+    else:
+        x1 = x[..., :half]
+        x2 = x[..., half:]
     t1 = np.multiply(x1, c, dtype=np.float32)
     t2 = np.multiply(x2, s, dtype=np.float32)
     y1 = np.subtract(t1, t2, dtype=np.float32)
     t3 = np.multiply(x2, c, dtype=np.float32)
     t4 = np.multiply(x1, s, dtype=np.float32)
     y2 = np.add(t3, t4, dtype=np.float32)
+    if interleaved:
+        y = np.empty_like(x)
+        y[..., 0::2] = y1
+        y[..., 1::2] = y2
+        return f32_to_t(y, dtype)
     return f32_to_t(np.concatenate([y1, y2], axis=-1), dtype)
 
 
@@ -197,12 +207,13 @@ def check_lengths(seqlens_k, seq_len, max_seq_len, total_sequence_length) -> int
 
 def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length,
                 cos_cache, sin_cache, num_heads, kv_num_heads, scale, local_window_size,
-                attention_bias, dtype, batches=None, heads=None):
+                attention_bias, dtype, batches=None, heads=None, interleaved=False):
     """Returns (status, out, k_buf_new, v_buf_new).
 
     query [B, S, H*D], key/value [B, S, Hkv*D], k_buf/v_buf [B, Hkv, M, D],
     cos/sin [rows, D/2] or None (no rotary), attention_bias [Bb, Hb, S, total]
-    or None.  ``out`` is float64 [B, S, H*D] (unrounded); on an error the
+    or None; ``interleaved`` selects the rotary pairing.  ``out`` is float64
+    [B, S, H*D] (unrounded); on an error the
     buffers come back unchanged and ``out`` is None.  scale <= 0 means
     1/sqrt(D); the scale is taken as a float32 value, as the operator's
     attribute is."""
@@ -218,8 +229,8 @@ def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_lengt
     v = value.reshape(B, S, Hkv, D)
     if cos_cache is not None:
         pos = positions(seqlens_k, S)
-        q = rotary(q, pos, cos_cache, sin_cache, dtype)
-        k = rotary(k, pos, cos_cache, sin_cache, dtype)
+        q = rotary(q, pos, cos_cache, sin_cache, dtype, interleaved)
+        k = rotary(k, pos, cos_cache, sin_cache, dtype, interleaved)
     kb = scatter_append(k_buf, k, seqlens_k)
     vb = scatter_append(v_buf, v, seqlens_k)
     out = attention(q, kb, vb, seqlens_k, H, Hkv, scale, local_window_size, attention_bias,

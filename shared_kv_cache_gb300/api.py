@@ -1,0 +1,57 @@
+"""Tensor-level convenience over gqa_forward: derives the dims from torch
+tensor shapes, keeps a reusable workspace, and raises on a non-OK status.
+Marshalling only; the CUDA library does the work."""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _binding as B
+
+_DT = {torch.float16: B.GQA_DTYPE_FP16, torch.bfloat16: B.GQA_DTYPE_BF16}
+
+
+class Workspace:
+    """A grow-only device scratch buffer for gqa_forward."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int, device) -> Optional[torch.Tensor]:
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes or self.buf.device != torch.device(device):
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        return self.buf
+
+
+def dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache=None, attention_bias=None,
+             rotary_interleaved=0):
+    Bsz, S, HD = query.shape
+    D = HD // num_heads
+    M = k_buf.shape[2]
+    bb, bh = (attention_bias.shape[0], attention_bias.shape[1]) if attention_bias is not None else (1, 1)
+    rows = cos_cache.shape[0] if cos_cache is not None else 0
+    return B.make_dims(Bsz, S, num_heads, kv_num_heads, D, M, _DT[query.dtype], rotary_interleaved, rows, bb, bh)
+
+
+def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, num_heads, kv_num_heads,
+            cos_cache=None, sin_cache=None, scale=0.0, local_window_size=0, attention_bias=None,
+            output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
+    """One GroupQueryAttention step; k_buf/v_buf are updated in place (the
+    shared past/present binding).  Returns the output tensor [B, S, H*D]."""
+    dims = dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias, rotary_interleaved)
+    nbytes = B.gqa_workspace_size(dims, total_sequence_length, local_window_size)
+    ws = (workspace or Workspace()).get(nbytes, query.device)
+    if output is None:
+        output = torch.empty_like(query)
+    if stream is None:
+        stream = torch.cuda.current_stream(query.device)
+    st = B.gqa_forward(dims, query, key, value, k_buf, v_buf, k_buf, v_buf, seqlens_k, total_sequence_length,
+                       cos_cache, sin_cache, scale, local_window_size, attention_bias, output, ws,
+                       0 if ws is None else ws.numel(), stream)
+    if st != B.GQA_OK:
+        raise B.GqaError(st)
+    return output

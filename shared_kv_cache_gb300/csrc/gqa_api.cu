@@ -1,0 +1,253 @@
+// libgqa host side: argument validation, the kernel plan, dispatch, and the
+// device error word.  Every check that the host can make runs before any
+// launch, so a rejected call leaves every buffer untouched (the operator
+// "shall fail" when the buffer has no room -- "Clarification about
+// GroupQueryAttention behavior", tianleiwu's reply).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gqa {
+
+// The device error word (one per device that loads the library).
+__device__ int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+int* error_word_ptr() {
+  static std::atomic<int*> cache[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  int* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_error_word) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(a);
+    cache[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 152;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// Checks the dims alone.
+gqa_status_t check_dims(const gqa_dims_t* d) {
+  if (!d) return GQA_ERR_INVALID_ARGUMENT;
+  if (d->batch < 1 || d->seq_len < 1 || d->num_heads < 1 || d->kv_num_heads < 1 || d->max_seq_len < 1)
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (d->num_heads % d->kv_num_heads != 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (d->head_size < 8 || d->head_size > 256 || d->head_size % 8 != 0) return GQA_ERR_INVALID_ARGUMENT;
+  if (d->dtype != GQA_DTYPE_FP16 && d->dtype != GQA_DTYPE_BF16) return GQA_ERR_INVALID_ARGUMENT;
+  if (d->rotary_interleaved != 0 && d->rotary_interleaved != 1) return GQA_ERR_INVALID_ARGUMENT;
+  // every index the kernels form stays within 32-bit row counts / 64-bit bytes
+  const long long rows = (long long)d->batch * d->kv_num_heads * d->max_seq_len;
+  if (rows >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+  if ((long long)d->batch * d->seq_len * d->num_heads >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
+  return GQA_OK;
+}
+
+}  // namespace
+
+Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms) {
+  Plan pl{};
+  const int G = H / Hkv;
+  if (S == 1 && D == 128 && G <= kDecodeMaxGroup) {
+    pl.path = Path::kDecode;
+    const long long leff = window > 0 ? std::min(total, window) : total;
+    // Aim for about four waves of two CTAs per SM when sequences are on
+    // average half the longest length; chunks are whole tiles.
+    const long long est_rows = (long long)B * Hkv * leff / 2;
+    const long long target = 8LL * num_sms;
+    long long chunk = (est_rows + target - 1) / target;
+    chunk = (chunk + kDecodeTile - 1) / kDecodeTile * kDecodeTile;
+    chunk = std::max<long long>(kDecodeTile, std::min<long long>(chunk, 4096));
+    pl.chunk = (int)chunk;
+    pl.nsplit = (int)((leff + chunk - 1) / chunk);
+    if (pl.nsplit < 1) pl.nsplit = 1;
+    size_t off = 0;
+    if (pl.nsplit > 1) {
+      pl.part_o_off = off;
+      pl.part_o_bytes = (size_t)B * H * pl.nsplit * D * sizeof(float);
+      off = align_up(off + pl.part_o_bytes, 256);
+      pl.part_ml_off = off;
+      pl.part_ml_bytes = (size_t)B * H * pl.nsplit * 2 * sizeof(float);
+      off = align_up(off + pl.part_ml_bytes, 256);
+    }
+    pl.total_bytes = off;
+    return pl;
+  }
+  pl.path = Path::kGeneric;
+  if (rotary) {
+    pl.q_rot_off = 0;
+    pl.q_rot_bytes = (size_t)B * S * H * D * 2;
+    pl.total_bytes = align_up(pl.q_rot_bytes, 256);
+  }
+  return pl;
+}
+
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                       CUtensorMapSwizzle swizzle) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  if (!fn) return false;
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(map, type, rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace gqa
+
+using namespace gqa;
+
+extern "C" {
+
+const char* gqa_status_string(gqa_status_t s) {
+  switch (s) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARGUMENT: return "GQA_ERR_INVALID_ARGUMENT";
+    case GQA_ERR_KV_OVERFLOW: return "GQA_ERR_KV_OVERFLOW";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+    case GQA_ERR_TIMEOUT: return "GQA_ERR_TIMEOUT";
+  }
+  return "GQA_ERR_UNKNOWN";
+}
+
+size_t gqa_workspace_size(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size) {
+  if (check_dims(dims) != GQA_OK || total_sequence_length < dims->seq_len) return 0;
+  const Plan pl = make_plan(dims->batch, dims->seq_len, dims->num_heads, dims->kv_num_heads, dims->head_size,
+                            total_sequence_length, local_window_size, true, sm_count());
+  return pl.total_bytes;
+}
+
+gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
+                         const void* past_key, const void* past_value, void* present_key, void* present_value,
+                         const int32_t* seqlens_k, int32_t total_sequence_length, const void* cos_cache,
+                         const void* sin_cache, float scale, int32_t local_window_size,
+                         const void* attention_bias, void* output, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  gqa_status_t st = check_dims(dims);
+  if (st != GQA_OK) return st;
+  const int B = dims->batch, S = dims->seq_len, H = dims->num_heads, Hkv = dims->kv_num_heads;
+  const int D = dims->head_size, M = dims->max_seq_len;
+
+  // packed QKV (key and value absent) is a form this library does not take
+  if (!key && !value) return GQA_ERR_UNSUPPORTED;
+  if (!query || !key || !value || !past_key || !past_value || !present_key || !present_value || !seqlens_k ||
+      !output)
+    return GQA_ERR_INVALID_ARGUMENT;
+  // the shared binding: past and present are one tensor
+  if (past_key != present_key || past_value != present_value) return GQA_ERR_UNSUPPORTED;
+  if (present_key == present_value) return GQA_ERR_INVALID_ARGUMENT;
+  if (misaligned(query) || misaligned(key) || misaligned(value) || misaligned(present_key) ||
+      misaligned(present_value) || misaligned(output) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (total_sequence_length < S) return GQA_ERR_INVALID_ARGUMENT;
+  if (total_sequence_length > M) return GQA_ERR_KV_OVERFLOW;
+  if ((cos_cache == nullptr) != (sin_cache == nullptr)) return GQA_ERR_INVALID_ARGUMENT;
+  if (cos_cache) {
+    if (misaligned(cos_cache) || misaligned(sin_cache)) return GQA_ERR_INVALID_ARGUMENT;
+    if (dims->cos_cache_rows < total_sequence_length) return GQA_ERR_INVALID_ARGUMENT;
+  }
+  if (attention_bias) {
+    if (dims->bias_batch != 1 && dims->bias_batch != B) return GQA_ERR_INVALID_ARGUMENT;
+    if (dims->bias_heads != 1 && dims->bias_heads != H) return GQA_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(attention_bias) & 1u) return GQA_ERR_INVALID_ARGUMENT;
+  }
+  if (!(std::isfinite(scale))) return GQA_ERR_INVALID_ARGUMENT;
+
+  const int nsm = sm_count();
+  const Plan pl = make_plan(B, S, H, Hkv, D, total_sequence_length, local_window_size, cos_cache != nullptr, nsm);
+  if (workspace_bytes < pl.total_bytes || (pl.total_bytes > 0 && !workspace)) return GQA_ERR_INVALID_ARGUMENT;
+  if (pl.total_bytes > 0 && misaligned(workspace)) return GQA_ERR_INVALID_ARGUMENT;
+
+  int* err = error_word_ptr();
+  if (!err) return GQA_ERR_CUDA;
+
+  ForwardArgs a{};
+  a.B = B; a.S = S; a.H = H; a.Hkv = Hkv; a.D = D; a.M = M;
+  a.dtype = dims->dtype;
+  a.interleaved = dims->rotary_interleaved;
+  a.total = total_sequence_length;
+  a.window = local_window_size > 0 ? local_window_size : 0;
+  a.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
+  a.q = query; a.k = key; a.v = value;
+  a.kbuf = present_key; a.vbuf = present_value;
+  a.seqlens = seqlens_k;
+  a.cos = cos_cache; a.sin = sin_cache;
+  a.bias = attention_bias;
+  a.bias_b = attention_bias ? dims->bias_batch : 1;
+  a.bias_h = attention_bias ? dims->bias_heads : 1;
+  a.out = output;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.err = err;
+  a.num_sms = nsm;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaSuccess;
+  switch (pl.path) {
+    case Path::kDecode:
+      e = launch_decode(a, pl, reinterpret_cast<float*>(ws + pl.part_o_off),
+                        reinterpret_cast<float*>(ws + pl.part_ml_off));
+      break;
+    case Path::kPrefillTC:
+    case Path::kGeneric: {
+      void* q_rot = cos_cache ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
+      e = launch_rope_append(a, q_rot);
+      if (e == cudaSuccess) e = launch_attn_generic(a, q_rot ? q_rot : query);
+      break;
+    }
+  }
+  return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+gqa_status_t gqa_check_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpyFromSymbol(&h, g_error_word, sizeof(int)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (h != 0) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &z, sizeof(int)) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return static_cast<gqa_status_t>(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// Host-side interfaces between the C-ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gqa.h"
+
+namespace gqa {
+
+// Everything one gqa_forward call needs, validated and resolved.
+struct ForwardArgs {
+  int B, S, H, Hkv, D, M;
+  int dtype;        // gqa_dtype_t
+  int interleaved;  // rotary pairing
+  int total;        // total_sequence_length
+  int window;       // <= 0: none
+  float scale;      // resolved (> 0)
+  const void* q;
+  const void* k;
+  const void* v;
+  void* kbuf;
+  void* vbuf;
+  const int32_t* seqlens;
+  const void* cos;  // nullptr: no rotary
+  const void* sin;
+  const void* bias;  // nullptr: none
+  int bias_b, bias_h;
+  void* out;
+  cudaStream_t stream;
+  int* err;  // device error word
+  int num_sms;
+};
+
+enum class Path { kDecode, kPrefillTC, kGeneric };
+
+// Which kernels run and how the workspace is carved up.  Derived from the
+// dims alone, so gqa_workspace_size() and gqa_forward() agree.
+struct Plan {
+  Path path;
+  int chunk = 0;   // decode: keys per split (multiple of the tile)
+  int nsplit = 0;  // decode: splits per (sequence, KV head) at the longest length
+  size_t q_rot_off = 0, q_rot_bytes = 0;    // rotated queries, T [B, S, H, D]
+  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [B, H, nsplit, D]
+  size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [B, H, nsplit, 2]
+  size_t total_bytes = 0;
+};
+
+Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms);
+
+// Kernel launchers (each returns the launch's cudaError_t).
+cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot);
+cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src);
+cudaError_t launch_decode(const ForwardArgs& a, const Plan& plan, float* part_o, float* part_ml);
+cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src);
+
+// Tensor-map encoding through the driver entry point (no libcuda link).
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                       CUtensorMapSwizzle swizzle);
+
+// Decode kernel geometry shared by the plan and the launcher.
+constexpr int kDecodeTile = 64;     // keys per pipeline stage
+constexpr int kDecodeMaxGroup = 16;  // query heads per KV head the decode kernel supports
+
+}  // namespace gqa

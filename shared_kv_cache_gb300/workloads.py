@@ -95,47 +95,56 @@ def draw_past(w: Workload, gen: torch.Generator) -> torch.Tensor:
 
 
 def make_inputs(w: Workload, seed: Optional[int] = None, sentinel: bool = True,
-                fill_past: bool = True) -> dict:
-    """Draw one batch of inputs for workload ``w`` on the CPU.
+                fill_past: bool = True, device: str = "cpu") -> dict:
+    """Draw one batch of inputs for workload ``w``.
 
     Q/K/V and the past region of the buffer are N(0, 1); the bias is
     N(0, bias_std).  Buffer slots at or beyond each sequence's past length hold
-    the NaN sentinel when ``sentinel`` is set, zeros otherwise."""
+    the NaN sentinel when ``sentinel`` is set, zeros otherwise.  The past
+    lengths always come from a CPU generator; with ``device`` other than
+    "cpu" the bulk tensors are drawn there (same distributions, other
+    values), which is much faster for the large buffers."""
     seed = w.seed if seed is None else seed
     gen = torch.Generator().manual_seed(seed)
+    dgen = gen if device == "cpu" else torch.Generator(device).manual_seed(seed)
     t = DTYPES[w.dtype]
     B, S, H, Hkv, D, M = w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len
     past = draw_past(w, gen)
     total = w.total_sequence_length if w.total_sequence_length is not None else int(past.max()) + S
 
-    q = torch.randn(B, S, H * D, generator=gen).to(t)
-    k = torch.randn(B, S, Hkv * D, generator=gen).to(t)
-    v = torch.randn(B, S, Hkv * D, generator=gen).to(t)
+    def randn(*shape):
+        return torch.randn(*shape, generator=dgen, device=device)
+
+    q = randn(B, S, H * D).to(t)
+    k = randn(B, S, Hkv * D).to(t)
+    v = randn(B, S, Hkv * D).to(t)
 
     bufs = []
     for _ in range(2):
         if sentinel:
-            buf = torch.full((B, Hkv, M, D), SENTINEL_BITS[w.dtype], dtype=torch.int16).view(t)
+            buf = torch.full((B, Hkv, M, D), SENTINEL_BITS[w.dtype], dtype=torch.int16, device=device).view(t)
         else:
-            buf = torch.zeros(B, Hkv, M, D, dtype=t)
+            buf = torch.zeros(B, Hkv, M, D, dtype=t, device=device)
         if fill_past:
             for b in range(B):
                 n = int(past[b])
                 if n > 0:
-                    buf[b, :, :n, :] = torch.randn(Hkv, n, D, generator=gen).to(t)
+                    buf[b, :, :n, :] = randn(Hkv, n, D).to(t)
         bufs.append(buf)
 
     rows = max(total, M)
     cos, sin = rotary_cache(rows, D, w.dtype) if w.rotary else (None, None)
+    if cos is not None and device != "cpu":
+        cos, sin = cos.to(device), sin.to(device)
 
     bias = None
     if w.bias_shape is not None:
         Bb, Hb = w.bias_shape
-        bias = (torch.randn(Bb, Hb, S, total, generator=gen) * w.bias_std).to(t)
+        bias = (randn(Bb, Hb, S, total) * w.bias_std).to(t)
 
     return {
         "workload": w, "query": q, "key": k, "value": v,
-        "k_buf": bufs[0], "v_buf": bufs[1], "seqlens_k": past,
+        "k_buf": bufs[0], "v_buf": bufs[1], "seqlens_k": past.to(device),
         "total_sequence_length": int(total), "cos": cos, "sin": sin,
         "attention_bias": bias, "scale": 1.0 / math.sqrt(D),
         "local_window_size": w.local_window_size,

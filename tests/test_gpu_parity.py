@@ -1,0 +1,168 @@
+"""CUDA path versus the CPU oracle, through the C ABI, on seeded inputs.
+
+KV append: bit-exact over the whole buffer (slots outside the new tokens keep
+their NaN sentinel or past values).  Attention output: max-abs error within
+2e-3 (fp16) / 1e-2 (bf16) of the oracle's float64 result."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import shared_kv_cache_gb300 as gqa
+from shared_kv_cache_gb300 import workloads as W
+
+from gqa_cases import compare, run_cuda, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    gqa.load_library()
+
+
+def custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999), seed=7, bias=None,
+           window=0, total=None, rotary=True, interleaved=0, sentinel=True):
+    w = W.Workload("custom", dtype, B, S, H, Hkv, D, M, 0, 0, bias_shape=bias, local_window_size=window,
+                   total_sequence_length=total, rotary=rotary, seed=seed)
+    inp = W.make_inputs(w, sentinel=sentinel, fill_past=False)
+    inp["seqlens_k"] = torch.tensor(past, dtype=torch.int32)
+    gen = torch.Generator().manual_seed(seed + 1000)
+    for name in ("k_buf", "v_buf"):
+        for b, n in enumerate(past):
+            if n > 0:
+                inp[name][b, :, :n] = torch.randn(Hkv, n, D, generator=gen).to(W.DTYPES[dtype])
+    t = total if total is not None else max(past) + S
+    inp["total_sequence_length"] = t
+    if rotary:
+        inp["cos"], inp["sin"] = W.rotary_cache(max(t, M), D, dtype)
+    if bias is not None:
+        inp["attention_bias"] = (torch.randn(bias[0], bias[1], S, t, generator=gen) * 0.5).to(W.DTYPES[dtype])
+    inp["rotary_interleaved"] = interleaved
+    return inp
+
+
+def check(inp, heads=None, batches=None):
+    res = run_cuda(inp)
+    ref = run_oracle(inp, heads=heads, batches=batches)
+    return compare(inp, res, ref, heads=heads, batches=batches)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads at their full sizes
+# ---------------------------------------------------------------------------
+def test_tiny_prefill_then_decode():
+    """32-token prompt (head size 8) into an empty past, then one decode token
+    over the grown sequence of 33."""
+    w = W.CONFIGS["tiny_prefill"]
+    inp = W.make_inputs(w)
+    res = run_cuda(inp)
+    ref = run_oracle(inp)
+    compare(inp, res, ref)
+    wd = W.CONFIGS["tiny_decode"]
+    dec = W.make_inputs(wd, seed=1)
+    dec["k_buf"] = res[3].clone()
+    dec["v_buf"] = res[4].clone()
+    dec["seqlens_k"] = torch.tensor([32], dtype=torch.int32)
+    dec["total_sequence_length"] = 33
+    compare(dec, run_cuda(dec), run_oracle(dec))
+
+
+def test_decode_b16_full():
+    check(W.make_inputs(W.CONFIGS["decode_b16"]))
+
+
+def test_prefill_2k_full_sampled_heads():
+    check(W.make_inputs(W.CONFIGS["prefill_2k"]), heads=[0, 7, 12, 31])
+
+
+def test_chunked_prefill_full_with_bias():
+    check(W.make_inputs(W.CONFIGS["chunked_prefill"]), heads=[0, 3, 17, 30])
+
+
+@pytest.mark.parametrize("name", ["long_decode", "long_decode_w4096"])
+def test_long_decode_full_sampled_heads(name):
+    check(W.make_inputs(W.CONFIGS[name]), heads=[0, 9, 37, 63])
+
+
+def test_chunked_overflow_is_an_error_and_writes_nothing():
+    w = W.CONFIGS["chunked_overflow"]
+    inp = W.make_inputs(w)
+    kb0, vb0 = W.bits(inp["k_buf"]).copy(), W.bits(inp["v_buf"]).copy()
+    # host-visible: total_sequence_length = past + new = 4128 > max_seq_len
+    st, dst, out, kb, vb = run_cuda(inp, total=4128)
+    assert st == gqa.GQA_ERR_KV_OVERFLOW and dst == gqa.GQA_OK
+    assert np.array_equal(W.bits(kb), kb0) and np.array_equal(W.bits(vb), vb0)
+    # device-visible: the host is told total = 4096, seqlens_k says 4000 + 128
+    st, dst, out, kb, vb = run_cuda(inp)
+    assert st == gqa.GQA_OK and dst == gqa.GQA_ERR_KV_OVERFLOW
+    assert np.array_equal(W.bits(kb), kb0) and np.array_equal(W.bits(vb), vb0)
+    assert torch.isnan(out.float()).all()   # no output row written for the skipped sequence
+    assert run_oracle(inp, total_sequence_length=4128)[0] == oracle.STATUS_KV_OVERFLOW
+
+
+# ---------------------------------------------------------------------------
+# Decode path: ragged lengths, tails, windows, bias, group sizes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(dtype="fp16"),
+    dict(past=(0, 1, 63, 64, 65, 127, 128, 999), B=8, seed=8),
+    dict(H=16, Hkv=1, seed=9),                      # G = 16
+    dict(H=4, Hkv=4, seed=10),                      # G = 1 (MHA)
+    dict(H=12, Hkv=4, seed=11),                     # G = 3
+    dict(window=100, seed=12),
+    dict(window=1, seed=13),
+    dict(window=64, past=(63, 64, 200), seed=14),
+    dict(bias=(1, 1), seed=15),
+    dict(bias=(3, 8), dtype="fp16", seed=16),
+    dict(rotary=False, seed=17),
+    dict(interleaved=1, seed=18),
+    dict(M=4096, past=(4095, 3000, 17), total=4096, seed=19),   # the last slot of the buffer
+])
+def test_decode_cases(kw):
+    check(custom(**kw))
+
+
+def test_decode_device_overflow_skips_that_sequence():
+    inp = custom(M=600, past=(10, 600, 300), total=600, seed=20)
+    kb0, vb0 = W.bits(inp["k_buf"]).copy(), W.bits(inp["v_buf"]).copy()
+    st, dst, out, kb, vb = run_cuda(inp)
+    assert st == gqa.GQA_OK and dst == gqa.GQA_ERR_KV_OVERFLOW
+    assert np.array_equal(W.bits(kb)[1], kb0[1]) and np.array_equal(W.bits(vb)[1], vb0[1])
+    assert torch.isnan(out[1].float()).all()
+    # the other sequences are computed as usual
+    ok = custom(M=600, past=(10, 300), total=600, seed=20, B=2)
+    ok["query"], ok["key"], ok["value"] = (inp[n][[0, 2]].contiguous() for n in ("query", "key", "value"))
+    ok["k_buf"], ok["v_buf"] = inp["k_buf"][[0, 2]].contiguous(), inp["v_buf"][[0, 2]].contiguous()
+    ref = run_oracle(ok)
+    assert np.array_equal(W.bits(kb)[[0, 2]], ref[2]) and np.array_equal(W.bits(vb)[[0, 2]], ref[3])
+    got = out[[0, 2]].double().numpy()
+    assert np.abs(got - ref[1]).max() <= 1e-2
+
+
+def test_decode_repeat_is_idempotent():
+    inp = custom(seed=21)
+    a = run_cuda(inp)
+    b = run_cuda(inp)
+    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+
+
+# ---------------------------------------------------------------------------
+# Prefill / generic path
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("kw", [
+    dict(S=37, past=(0, 5, 90), M=160, dtype="fp16", seed=30),
+    dict(S=37, past=(0, 5, 90), M=160, dtype="bf16", bias=(3, 8), seed=31),
+    dict(S=130, past=(0, 129, 7), M=300, window=50, seed=32),
+    dict(S=5, D=64, past=(3, 0, 40), M=64, seed=33),
+    dict(S=5, D=256, past=(3, 0, 40), M=64, seed=34),
+    dict(S=9, D=24, H=6, Hkv=3, past=(1, 2, 3), M=16, seed=35),
+    dict(S=1, D=64, past=(3, 0, 40), M=64, seed=36),
+    dict(S=16, D=8, H=4, Hkv=2, past=(0, 4, 8), M=32, interleaved=1, seed=37),
+    dict(S=16, D=128, rotary=False, past=(0, 4, 8), M=32, seed=38),
+])
+def test_prefill_cases(kw):
+    check(custom(**kw))

@@ -1,0 +1,122 @@
+"""Host-side tests of the C ABI that need no GPU: the library loads, exports
+every entry point its header declares, and rejects bad arguments before any
+launch (so no device memory is touched; the pointers below are never
+dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import shared_kv_cache_gb300 as gqa
+from shared_kv_cache_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gqa.load_library()
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gqa_[a-z_0-9]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = header_functions()
+    assert {"gqa_forward", "gqa_workspace_size", "gqa_check_device_status", "gqa_status_string"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "GQA_OK"), (1, "GQA_ERR_INVALID_ARGUMENT"), (2, "GQA_ERR_KV_OVERFLOW"),
+                       (3, "GQA_ERR_UNSUPPORTED"), (4, "GQA_ERR_CUDA"), (5, "GQA_ERR_TIMEOUT")]:
+        assert gqa.gqa_status_string(code) == name
+
+
+# fake, 16-byte aligned device addresses: every call below fails validation first
+P = {n: 0x10000 * (i + 1) for i, n in enumerate(
+    ["q", "k", "v", "kb", "vb", "seq", "cos", "sin", "bias", "out", "ws"])}
+
+
+def call(dims, total=64, **over):
+    a = dict(query=P["q"], key=P["k"], value=P["v"], past_key=P["kb"], past_value=P["vb"],
+             present_key=P["kb"], present_value=P["vb"], seqlens_k=P["seq"], total_sequence_length=total,
+             cos_cache=P["cos"], sin_cache=P["sin"], scale=0.0, local_window_size=0, attention_bias=None,
+             output=P["out"], workspace=P["ws"], workspace_bytes=1 << 30)
+    a.update(over)
+    return gqa.gqa_forward(dims, **a)
+
+
+def dims(**over):
+    d = dict(batch=2, seq_len=4, num_heads=8, kv_num_heads=2, head_size=64, max_seq_len=128, dtype="fp16",
+             rotary_interleaved=0, cos_cache_rows=128, bias_batch=1, bias_heads=1)
+    d.update(over)
+    return gqa.make_dims(**d)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(batch=0), dict(seq_len=0), dict(num_heads=6, kv_num_heads=4), dict(head_size=12),
+    dict(head_size=264), dict(head_size=0), dict(max_seq_len=0), dict(dtype=7), dict(rotary_interleaved=2),
+    dict(kv_num_heads=0),
+])
+def test_bad_dims_rejected(lib, bad):
+    assert call(dims(**bad)) == gqa.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_overflow_rejected_before_launch(lib):
+    # total_sequence_length beyond the buffer: the operator fails
+    assert call(dims(max_seq_len=128), total=129) == gqa.GQA_ERR_KV_OVERFLOW
+    assert call(dims(max_seq_len=4096, seq_len=128), total=4128) == gqa.GQA_ERR_KV_OVERFLOW
+
+
+def test_shared_binding_required(lib):
+    assert call(dims(), present_key=P["kb"] + 4096) == gqa.GQA_ERR_UNSUPPORTED
+    assert call(dims(), present_value=P["vb"] + 4096) == gqa.GQA_ERR_UNSUPPORTED
+
+
+def test_pointer_checks(lib):
+    assert call(dims(), key=None, value=None) == gqa.GQA_ERR_UNSUPPORTED          # packed QKV
+    assert call(dims(), key=None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), query=None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), output=None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), seqlens_k=None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), query=P["q"] + 2) == gqa.GQA_ERR_INVALID_ARGUMENT          # misaligned
+    assert call(dims(), sin_cache=None) == gqa.GQA_ERR_INVALID_ARGUMENT            # half a rotary pair
+    assert call(dims(), present_value=P["kb"], past_value=P["kb"]) == gqa.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_length_and_cache_checks(lib):
+    assert call(dims(seq_len=8), total=7) == gqa.GQA_ERR_INVALID_ARGUMENT         # total < S
+    assert call(dims(cos_cache_rows=32), total=64) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(bias_batch=3), attention_bias=P["bias"]) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(bias_heads=2), attention_bias=P["bias"]) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), scale=float("nan")) == gqa.GQA_ERR_INVALID_ARGUMENT
+
+
+def test_workspace_checks(lib):
+    d = dims()
+    need = gqa.gqa_workspace_size(d, 64, 0)
+    assert need > 0
+    assert call(d, workspace_bytes=need - 1) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(d, workspace=None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert gqa.gqa_workspace_size(dims(batch=0), 64, 0) == 0
+
+
+def test_workspace_plan_decode(lib):
+    # decode at D = 128 uses split-KV partials; one split needs no scratch
+    d = dims(seq_len=1, head_size=128, num_heads=32, kv_num_heads=8, batch=16, max_seq_len=4096)
+    big = gqa.gqa_workspace_size(d, 4096, 0)
+    assert big > 0 and big % 256 == 0
+    d1 = dims(seq_len=1, head_size=128, num_heads=4, kv_num_heads=4, batch=1, max_seq_len=64)
+    assert gqa.gqa_workspace_size(d1, 33, 0) == 0

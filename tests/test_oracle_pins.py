@@ -102,6 +102,30 @@ def test_rotary_is_complex_rotation(dtype):
 
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_rotary_interleaved_is_complex_rotation(dtype):
+    """Interleaved layout: pair j is z = x[2j] + i x[2j+1], rotated by
+    cos + i sin of cache entry j."""
+    r = _rng(4)
+    B, S, Hh, D = 1, 3, 2, 16
+    x = _tbits(r.standard_normal((B, S, Hh, D)), dtype)
+    cos, sin = W.rotary_cache(32, D, dtype)
+    cos, sin = W.bits(cos), W.bits(sin)
+    pos = oracle.positions(np.array([7]), S)
+    y = oracle.t_to_f64(oracle.rotary(x, pos, cos, sin, dtype, interleaved=True), dtype)
+    xf = oracle.t_to_f64(x, dtype)
+    c = oracle.t_to_f64(cos, dtype)[pos][:, :, None, :]
+    s = oracle.t_to_f64(sin, dtype)[pos][:, :, None, :]
+    z = (xf[..., 0::2] + 1j * xf[..., 1::2]) * (c + 1j * s)
+    exact = np.empty_like(xf)
+    exact[..., 0::2] = z.real
+    exact[..., 1::2] = z.imag
+    ulp = np.spacing(np.abs(exact).astype(np.float16 if dtype == "fp16" else np.float32)).astype(np.float64)
+    if dtype == "bf16":
+        ulp = ulp * 2 ** 16
+    assert np.all(np.abs(y - exact) <= ulp + 1e-30)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_rotary_position_zero_identity_and_norm(dtype):
     r = _rng(3)
     D = 128
