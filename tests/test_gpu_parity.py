@@ -147,7 +147,7 @@ def test_decode_repeat_is_idempotent():
     inp = custom(seed=21)
     a = run_cuda(inp)
     b = run_cuda(inp)
-    assert torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    assert all(np.array_equal(W.bits(x), W.bits(y)) for x, y in zip(a[2:], b[2:]))
 
 
 # ---------------------------------------------------------------------------
