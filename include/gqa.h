@@ -139,6 +139,40 @@ gqa_status_t gqa_check_device_status(void* stream);
 /* gqa_status_string -- a static, human-readable name for a status code. */
 const char* gqa_status_string(gqa_status_t status);
 
+/*
+ * gqa_decode_noalloc -- the decode step of gqa_forward (seq_len == 1,
+ * head_size == 128, at most 16 query heads per KV head) without a workspace
+ * argument.  The operator's pages have no counterpart to this entry point; it
+ * exists for callers that cannot allocate device memory when they run the
+ * step and have no scratch to pass -- for example an inference runtime whose
+ * memory planner hands out every buffer ahead of execution, or a serving
+ * loop in which cudaMalloc/cudaFree (which may synchronise the device) are
+ * not allowed.
+ *
+ * Arguments, layouts and error behaviour are those of gqa_forward, minus
+ * workspace/workspace_bytes.  The split-KV partial results go to a static
+ * device array of 16 MiB inside the library (held by every GPU that loads
+ * it, until exit); a call that would need more returns GQA_ERR_UNSUPPORTED
+ * before any launch, as do shapes other than the decode shape above.  The
+ * function allocates nothing.
+ *   - All calls on one device share that array and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls whose kernels
+ *     can overlap on the GPU race on it: order them on one stream.
+ *   - The first call on each device looks up the array's device address
+ *     with that device current; make that first call before any stream
+ *     capture begins.
+ */
+gqa_status_t gqa_decode_noalloc(const gqa_dims_t* dims,
+                                const void* query, const void* key, const void* value,
+                                const void* past_key, const void* past_value,
+                                void* present_key, void* present_value,
+                                const int32_t* seqlens_k, int32_t total_sequence_length,
+                                const void* cos_cache, const void* sin_cache,
+                                float scale, int32_t local_window_size,
+                                const void* attention_bias,
+                                void* output,
+                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,8 @@ GQA_ERR_TIMEOUT = 5
 GQA_DTYPE_FP16 = 0
 GQA_DTYPE_BF16 = 1
 
-EXPORTED = ("gqa_forward", "gqa_workspace_size", "gqa_check_device_status", "gqa_status_string")
+EXPORTED = ("gqa_forward", "gqa_workspace_size", "gqa_check_device_status", "gqa_status_string",
+            "gqa_decode_noalloc")
 
 
 class gqa_dims_t(ctypes.Structure):
@@ -56,6 +57,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_check_device_status.argtypes = [vp]
     lib.gqa_status_string.restype = ctypes.c_char_p
     lib.gqa_status_string.argtypes = [ctypes.c_int]
+    lib.gqa_decode_noalloc.restype = ctypes.c_int
+    lib.gqa_decode_noalloc.argtypes = [ctypes.POINTER(gqa_dims_t), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp,
+                                       f32, i32, vp, vp, vp]
     _lib = lib
     return lib
 
@@ -93,6 +97,19 @@ def gqa_forward(dims, query, key, value, past_key, past_value, present_key, pres
                            int(total_sequence_length), _ptr(cos_cache), _ptr(sin_cache), float(scale),
                            int(local_window_size), _ptr(attention_bias), _ptr(output), _ptr(workspace),
                            int(workspace_bytes), _stream(stream))
+
+
+def gqa_decode_noalloc(dims, query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
+                       total_sequence_length, cos_cache, sin_cache, scale, local_window_size, attention_bias,
+                       output, stream=None) -> int:
+    """The decode step without a workspace (for callers that cannot allocate
+    device memory when they run it): its scratch is a static 16 MiB device
+    array inside the library, shared by every call on the device."""
+    lib = load_library()
+    return lib.gqa_decode_noalloc(ctypes.byref(dims), _ptr(query), _ptr(key), _ptr(value), _ptr(past_key),
+                                  _ptr(past_value), _ptr(present_key), _ptr(present_value), _ptr(seqlens_k),
+                                  int(total_sequence_length), _ptr(cos_cache), _ptr(sin_cache), float(scale),
+                                  int(local_window_size), _ptr(attention_bias), _ptr(output), _stream(stream))
 
 
 def gqa_workspace_size(dims, total_sequence_length, local_window_size=0) -> int:

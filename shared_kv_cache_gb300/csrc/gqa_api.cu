@@ -76,6 +76,10 @@ gqa_status_t check_dims(const gqa_dims_t* d) {
 
 }  // namespace
 
+// Accessors for other translation units of the library.
+int* device_error_word() { return error_word_ptr(); }
+int device_sm_count() { return sm_count(); }
+
 Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms) {
   Plan pl{};
   const int G = H / Hkv;

@@ -50,6 +50,10 @@ struct Plan {
 
 Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms);
 
+// The current device's error word (device address) and SM count.
+int* device_error_word();
+int device_sm_count();
+
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot);
 cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src);
