@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--quick", action="store_true",
+                    help="headline workload only: no burn-in, end-to-end leg, other workloads or CPU baseline "
+                         "(for profiler runs)")
     return ap.parse_args()
 
 
@@ -323,7 +326,7 @@ def run_ours(args):
     # keep the GPU busy for ~1 s before timing so that the clock record reflects load
     tb = time.time()
     i = 0
-    while time.time() - tb < 1.0:
+    while not args.quick and time.time() - tb < 1.0:
         prob.step(i, stream)
         i += 1
         if i % 200 == 0:
@@ -335,7 +338,8 @@ def run_ours(args):
     gbs = prob.bytes / (ms * 1e-3) / 1e9
     value = gbs * ws
 
-    e2e_ms, h2d, d2h = e2e_decode(prob, args.steps, max(args.warmup, 3), stream)
+    e2e_ms, h2d, d2h = e2e_decode(prob, args.steps if not args.quick else 1, 1 if args.quick else
+                                  max(args.warmup, 3), stream)
     e2e = {"value": prob.bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
@@ -345,7 +349,7 @@ def run_ours(args):
                 "bytes_per_launch": prob.bytes, "traffic": None}
 
     also = []
-    if not args.no_also:
+    if not args.no_also and not args.quick:
         for name, sets in (("long_decode", 1), ("long_decode_w4096", 4), ("prefill_2k", 1),
                            ("chunked_prefill", 4)):
             p = Problem(name, device, sets=sets)
@@ -364,7 +368,7 @@ def run_ours(args):
             torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu:
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.quick:
         cpu = cpu_baseline(HEADLINE)
 
     w = prob.w

@@ -151,10 +151,10 @@ const char* gqa_status_string(gqa_status_t status);
  *
  * Arguments, layouts and error behaviour are those of gqa_forward, minus
  * workspace/workspace_bytes.  The split-KV partial results go to a static
- * device array of 16 MiB inside the library (held by every GPU that loads
- * it, until exit); a call that would need more returns GQA_ERR_UNSUPPORTED
- * before any launch, as do shapes other than the decode shape above.  The
- * function allocates nothing.
+ * device array of 4 MiB inside the library (held by every GPU that loads it,
+ * until exit; a 152-SM GB300 needs at most about 2.5 MB of it); a call that
+ * would need more returns GQA_ERR_UNSUPPORTED before any launch, as do shapes
+ * other than the decode shape above.  The function allocates nothing.
  *   - All calls on one device share that array and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose kernels
  *     can overlap on the GPU race on it: order them on one stream.

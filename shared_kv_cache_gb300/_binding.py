@@ -103,7 +103,7 @@ def gqa_decode_noalloc(dims, query, key, value, past_key, past_value, present_ke
                        total_sequence_length, cos_cache, sin_cache, scale, local_window_size, attention_bias,
                        output, stream=None) -> int:
     """The decode step without a workspace (for callers that cannot allocate
-    device memory when they run it): its scratch is a static 16 MiB device
+    device memory when they run it): its scratch is a static 4 MiB device
     array inside the library, shared by every call on the device."""
     lib = load_library()
     return lib.gqa_decode_noalloc(ctypes.byref(dims), _ptr(query), _ptr(key), _ptr(value), _ptr(past_key),

@@ -44,6 +44,12 @@ template <> struct Elem<__nv_bfloat16> {
   static constexpr bool is_bf16 = true;
 };
 
+// N elements of type T moved as one aligned vector.
+template <typename T, int N>
+struct alignas(sizeof(T) * N) VecT {
+  T v[N];
+};
+
 // ---------------------------------------------------------------------------
 // Rotary embedding of one pair in fp32, products first and no fused
 // multiply-add, so that the rounded result is reproducible bit for bit:
@@ -128,6 +134,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
   return true;
 }
 
+// 16-byte asynchronous global -> shared copy (cached in L2 only).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -205,7 +218,21 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
   }
 }
 
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
+// 2^x with the hardware approximation instruction (relative error ~2^-22;
+// 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Transpose of an 8x8 matrix of 16-bit values held one 32-bit register per
+// thread in the mma fragment layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -10,9 +10,12 @@
 // fixed static device array instead of a workspace.
 //
 // Limits and sharing:
-//   - The array holds kStaticScratchBytes (16 MiB); every GPU that loads the
-//     library keeps it until the process exits.  A call whose partials would
-//     not fit returns GQA_ERR_UNSUPPORTED before anything is launched.
+//   - The array holds kStaticScratchBytes (4 MiB); every GPU that loads the
+//     library keeps it until the process exits.  The decode kernels leave at
+//     most two partials of G x (128 + 2) floats per persistent CTA, about
+//     2.5 MB at most on a 152-SM GB300; a call whose partials would not fit
+//     (a device with far more SMs) returns GQA_ERR_UNSUPPORTED before
+//     anything is launched.
 //   - All calls on a device share the one array.  Calls whose kernels may
 //     overlap on the GPU (different streams without ordering, or several
 //     host threads) race on it; order them on one stream.
@@ -33,7 +36,7 @@
 namespace gqa {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 

@@ -1,29 +1,35 @@
 // Split-KV flash-decode for one new token per sequence (S = 1), D = 128.
 //
-// One CTA per (split s, KV head kh, sequence b).  It handles the keys
-// [lo + s*chunk, min(lo + (s+1)*chunk, L)) of that sequence, where
-// L = past_b + 1 is the true length and lo the window start: the scan stops
-// at the current length, never at max_seq_len ("KV Cache", rocMLIR
-// discussion, "Short summary of notes").  Splits that start at or beyond L
-// exit at once.
+// Work decomposition.  The keys each (sequence b, KV head kh) item must scan
+// run from the window start lo_b to the true length L_b = past_b + 1; the scan
+// stops there and never sweeps max_seq_len ("KV Cache", rocMLIR discussion,
+// "Short summary of notes").  Those keys are cut into 64-key tiles and the
+// tiles of all items are laid end to end, item after item.  The grid is
+// persistent (about two CTAs per SM) and CTA c takes the contiguous tile range
+// [c*T/P, (c+1)*T/P) of the T tiles, so every CTA streams the same number of
+// bytes however ragged the lengths are.  A range cuts items into segments:
+//   - an item that lies entirely inside one CTA is finished there (its output
+//     row is written directly);
+//   - an item cut by CTA boundaries leaves one fp32 partial (o, m, l) per CTA
+//     it touches -- at most two per CTA: "head" (slot 0) for an item that
+//     began in an earlier CTA, "tail" (slot 1) for one that begins in this CTA
+//     and runs on -- and the combine kernel below merges them.
 //
-// Fused into the same CTA: the rotary embedding of the G query rows of the
-// KV head, and -- in the CTA whose split holds the new token -- the rotary
-// embedding of the new key row and the scatter-append of the new K/V row at
-// slot past_b ("[TorchOnnxToTorch] Add pad+scatter KV cache and mask to GQA",
-// PR description).  The new row is also patched into the shared-memory tile,
-// so the TMA load never has to observe the global write.
+// Inside a CTA.  Warp 4 lane 0 streams [64 keys x 128] K and V tiles into a
+// 3-stage shared-memory ring with 2-D bulk-tensor copies (TMA, 128-byte
+// swizzle), running ahead across segment boundaries.  Warps 0..3 each own 16
+// keys of every tile and run S = Q K^T and O += P V with mma.sync m16n8k16:
+// the G query heads of the group are the rows of the A operand (padded to 16),
+// so every K/V tile loaded is reused by the whole group.  Softmax statistics
+// are reduced with quad shuffles; at the end of a segment warps 1..3 hand
+// their (m, l, O) to warp 0 through shared memory.
 //
-// Warp roles: warp 4 lane 0 streams [64 keys x 128] K and V tiles into a
-// 3-stage shared-memory ring with 2-D bulk-tensor copies (128-byte swizzle);
-// warps 0..3 each own 16 keys of every tile.  Each warp runs
-// S = Q K^T and O += P V with mma.sync m16n8k16: the G query heads of the
-// group are the 16 rows of the A operand (padded), so every loaded K/V tile
-// is reused by the whole group.  Softmax statistics are reduced with quad
-// shuffles; the four warps' partial results are merged through shared memory.
-// A sequence that needs more than one split writes fp32 partials (o, m, l)
-// that the combine kernel below merges; a single-split sequence writes its
-// output directly.
+// Fused steps.  Each segment rotates its G query rows at position past_b; the
+// CTA whose segment holds an item's last tile also rotates the new key row,
+// appends the new K/V row at slot past_b ("[TorchOnnxToTorch] Add pad+scatter
+// KV cache and mask to GQA", PR description: rotary at arange + past length,
+// scatter at seqlens_k) and patches that row into the shared-memory tile, so
+// the TMA load never has to observe the global write.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,20 +37,42 @@ namespace gqa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kTile = kDecodeTile;          // keys per stage
-constexpr int kCW = 4;                      // consumer warps (16 keys each)
+constexpr int kTile = kDecodeTile;           // keys per stage
+constexpr int kCW = 4;                       // consumer warps (16 keys each)
 constexpr int kStages = 3;
 constexpr int kThreads = (kCW + 1) * 32;
-constexpr int kBoxBytes = kTile * 128;      // one 64-column box of a tile
-constexpr int kTileBytes = 2 * kBoxBytes;   // K (or V) tile, 16 KB
+constexpr int kBoxBytes = kTile * 128;       // one 64-column box of a tile
+constexpr int kTileBytes = 2 * kBoxBytes;    // K (or V) tile, 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;  // K + V
-constexpr int kQStride = kD + 8;            // padded query row (elements)
+constexpr int kQStride = kD + 8;             // padded query row (elements)
 constexpr int kRing = kStages * kStageBytes;
-constexpr int kQOff = kRing;
-constexpr int kQBytes = 16 * kQStride * 2;
-constexpr int kNewOff = kQOff + kQBytes;    // staged new K row then V row
-constexpr int kBarOff = kNewOff + 2 * kD * 2;
-constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 1024;  // + alignment slack
+constexpr size_t kSmPerSM = 233472;          // shared memory per SM (bytes)
+constexpr size_t kSmReservedPerCta = 1024;
+constexpr int kSeqCache = 128;               // seqlens_k entries cached in shared memory
+
+// Shared-memory layout after the ring, for group size G.
+struct Layout {
+  int merge_warp_bytes;  // one warp's (O^T, m, l) hand-off
+  int merge_off;         // merge region: two hand-off slots (also holds the rotated query rows)
+  int stage_off;         // raw rows of the next segment, fetched with cp.async
+  int new_off;           // staged new K row then V row, rotated
+  int seq_off;           // seqlens_k cache (kSeqCache entries)
+  int bar_off;
+  int total;             // bytes, including 1 KB of alignment slack
+};
+__host__ __device__ constexpr Layout layout_for(int G) {
+  const int nt = G <= 8 ? 1 : 2;                        // 8-head column tiles
+  const int w = nt * (8 * 4 * 32 * 4 + 4 * 32 * 4);     // O^T fragments + (m, l) pairs, per lane
+  int merge = 2 * w;
+  const int qbytes = 16 * kQStride * 2;
+  if (merge < qbytes) merge = qbytes;
+  const int merge_off = kRing;
+  const int stage_off = merge_off + merge;
+  const int new_off = stage_off + nt * 8 * 256 + 4 * 128 + 2 * 256;
+  const int seq_off = new_off + 2 * kD * 2;
+  const int bar_off = seq_off + kSeqCache * 4;
+  return Layout{w, merge_off, stage_off, new_off, seq_off, bar_off, bar_off + 2 * kStages * 8 + 1024};
+}
 
 struct DecodeParams {
   const void* q;     // [B, 1, H*D]
@@ -57,10 +85,10 @@ struct DecodeParams {
   const void* sin;
   const void* bias;  // [Bb, Hb, 1, total] or nullptr
   void* out;         // [B, 1, H*D]
-  float* part_o;     // [B, H, nsplit, D]
-  float* part_ml;    // [B, H, nsplit, 2]
+  float* part_o;     // [P][2][G][D]
+  float* part_ml;    // [P][2][G][2]
   int* err;
-  int H, Hkv, G, M, total, window, chunk, nsplit, interleaved, bias_b, bias_h;
+  int B, H, Hkv, G, M, total, window, P, interleaved, bias_b, bias_h;
   float scale_log2;
 };
 
@@ -70,7 +98,75 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
   return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <typename T>
+// Keys of sequence b: [lo, L); returns its tile count (0 when the sequence
+// fails the length check and is skipped).
+__device__ __forceinline__ int seq_tiles(const DecodeParams& p, const int* sl, int b, int& lo, int& L) {
+  const int past = sl[b];
+  if (sequence_error(past, 1, p.M, p.total)) {
+    lo = L = 0;
+    return 0;
+  }
+  L = past + 1;
+  lo = p.window > 0 ? max(0, L - p.window) : 0;
+  return (L - lo + kTile - 1) / kTile;
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ long long warp_incl_scan_ll(long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// Warp-cooperative: total number of tiles over all items.
+__device__ long long total_tiles(const DecodeParams& p, const int* sl, int lane) {
+  long long t = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int lo, L;
+    const int b = b0 + lane;
+    const long long tb = b < p.B ? seq_tiles(p, sl, b, lo, L) : 0;
+    t += warp_sum_ll(tb);
+  }
+  return t * p.Hkv;
+}
+
+// Warp-cooperative: the sequence b whose items hold global tile x (x < T),
+// and the global index of the first tile of item (b, 0).
+__device__ void locate_seq(const DecodeParams& p, const int* sl, long long x, int lane, int& b_out,
+                           long long& start_out) {
+  long long base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int lo, L;
+    const int b = b0 + lane;
+    const long long tb = (b < p.B ? seq_tiles(p, sl, b, lo, L) : 0) * (long long)p.Hkv;
+    const long long incl = warp_incl_scan_ll(tb, lane);
+    const long long chunk = __shfl_sync(0xffffffffu, incl, 31);
+    if (x < base + chunk) {
+      const unsigned m = __ballot_sync(0xffffffffu, base + incl > x);
+      const int l = __ffs(m) - 1;
+      b_out = b0 + l;
+      start_out = base + __shfl_sync(0xffffffffu, incl - tb, l);
+      return;
+    }
+    base += chunk;
+  }
+  b_out = p.B;
+  start_out = base;
+}
+
+// CTA that owns global tile x.
+__device__ __forceinline__ int cta_of(long long x, long long T, int P) {
+  return (int)(((x + 1) * P - 1) / T);
+}
+
+template <typename T, int NT>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
@@ -78,32 +174,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr bool kBF16 = E::is_bf16;
   pdl_launch_dependents();
 
-  const int s = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
-  const int past = p.seqlens[b];
-  const int serr = sequence_error(past, 1, p.M, p.total);
-  if (serr) {
-    if (s == 0 && kh == 0 && threadIdx.x == 0) record_error(p.err, serr);
-    return;
-  }
-  const int L = past + 1;
-  const int lo = p.window > 0 ? max(0, L - p.window) : 0;
-  const int k0 = lo + s * p.chunk;
-  if (k0 >= L) return;
-  const int k1 = min(L, k0 + p.chunk);
-  const int ntiles = (k1 - k0 + kTile - 1) / kTile;
-  const int nsplit_b = (L - lo + p.chunk - 1) / p.chunk;
-  const bool has_new = (k1 == L);
   const int G = p.G;
-
+  const Layout lay = layout_for(G);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  T* qs = reinterpret_cast<T*>(smem + kQOff);
-  T* news = reinterpret_cast<T*>(smem + kNewOff);
-  const uint32_t bar_full = sbase + kBarOff;
+  T* qs = reinterpret_cast<T*>(smem + lay.merge_off);  // rotated query rows (aliases the merge region)
+  T* news = reinterpret_cast<T*>(smem + lay.new_off);
+  const uint32_t bar_full = sbase + lay.bar_off;
   const uint32_t bar_empty = bar_full + kStages * 8;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int* s_seq = reinterpret_cast<int*>(smem + lay.seq_off);
+  const bool cached = p.B <= kSeqCache;
+  if (cached)
+    for (int i = tid; i < p.B; i += kThreads) s_seq[i] = p.seqlens[i];
+  const int* sl = cached ? s_seq : p.seqlens;
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar_full + 8 * i, 1);
@@ -113,328 +199,607 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
 
+  // this CTA's tile range and the item holding its first tile
+  const long long Ttot = total_tiles(p, sl, lane);
+  const int c = blockIdx.x;
+  const long long lo_c = Ttot * c / p.P;
+  const long long hi_c = Ttot * (c + 1) / p.P;
+  if (lo_c >= hi_c) return;
+  int b;
+  long long sstart;  // first tile of item (b, 0)
+  locate_seq(p, sl, lo_c, lane, b, sstart);
+  int klo, L;
+  int tb = seq_tiles(p, sl, b, klo, L);
+  int kh = (int)((lo_c - sstart) / tb);
+  long long istart = sstart + (long long)kh * tb;
+
   if (warp == kCW) {
     // ---------------- producer ----------------
     if (lane == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      const int row0 = (b * p.Hkv + kh) * p.M + k0;
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kStages;
-        const int round = t / kStages;
-        if (round > 0 && !mbar_wait(bar_empty + 8 * st, (round - 1) & 1, p.err)) break;
-        const uint32_t fb = bar_full + 8 * st;
-        const uint32_t kd = sbase + st * kStageBytes;
-        const uint32_t vd = kd + kTileBytes;
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        const int y = row0 + t * kTile;
-        tma_load_2d(kd, &kmap, 0, y, fb);
-        tma_load_2d(kd + kBoxBytes, &kmap, 64, y, fb);
-        tma_load_2d(vd, &vmap, 0, y, fb);
-        tma_load_2d(vd + kBoxBytes, &vmap, 64, y, fb);
-        issued = t + 1;
+      long long x = lo_c;
+      int gt = 0;  // tiles issued by this CTA
+      bool ok = true;
+      while (ok && x < hi_c) {
+        const long long iend = istart + tb;
+        const long long send = iend < hi_c ? iend : hi_c;
+        const int row0 = (b * p.Hkv + kh) * p.M + klo;
+        for (long long t = x - istart; t < send - istart; ++t, ++gt) {
+          const int st = gt % kStages;
+          const int round = gt / kStages;
+          if (round > 0 && !mbar_wait(bar_empty + 8 * st, (round - 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * st;
+          const uint32_t kd = sbase + st * kStageBytes;
+          const uint32_t vd = kd + kTileBytes;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const int y = row0 + (int)t * kTile;
+          tma_load_2d(kd, &kmap, 0, y, fb);
+          tma_load_2d(kd + kBoxBytes, &kmap, 64, y, fb);
+          tma_load_2d(vd, &vmap, 0, y, fb);
+          tma_load_2d(vd + kBoxBytes, &vmap, 64, y, fb);
+        }
+        x = send;
+        if (x == iend && x < hi_c) {  // next item
+          istart = iend;
+          if (++kh == p.Hkv) {
+            kh = 0;
+            do {
+              ++b;
+              tb = seq_tiles(p, sl, b, klo, L);
+            } while (tb == 0);
+          }
+        }
       }
-      // Before leaving, make sure no copy into this CTA's shared memory is
-      // still in flight (the consumers wait on every issued tile in a normal
-      // run; after a timeout they may not have).
-      for (int t = max(0, issued - kStages); t < issued; ++t)
+      // Leave no copy in flight into this CTA's shared memory (after a
+      // timeout the consumers may not have waited for every tile).
+      for (int t = max(0, gt - kStages); t < gt; ++t)
         mbar_wait(bar_full + 8 * (t % kStages), (t / kStages) & 1, p.err);
     }
     return;
   }
 
   // ---------------- consumers (warps 0..3, 128 threads) ----------------
-  const T* qg = static_cast<const T*>(p.q) + ((size_t)b * p.H + (size_t)kh * G) * kD;
-  const bool rot = p.cos != nullptr;
-  const T* cosr = rot ? static_cast<const T*>(p.cos) + (size_t)past * (kD / 2) : nullptr;
-  const T* sinr = rot ? static_cast<const T*>(p.sin) + (size_t)past * (kD / 2) : nullptr;
-  // rotated query rows of the group into shared memory (rows >= G are zero)
-  for (int u = tid; u < 16 * (kD / 2); u += kCW * 32) {
-    const int g = u / (kD / 2), j = u % (kD / 2);
-    const int i1 = p.interleaved ? 2 * j : j;
-    const int i2 = p.interleaved ? 2 * j + 1 : j + kD / 2;
-    T y1 = E::from_f(0.f), y2 = E::from_f(0.f);
-    if (g < G) {
-      const T* qr = qg + (size_t)g * kD;
-      if (rot) {
-        float a, c;
-        rotate_pair(E::to_f(qr[i1]), E::to_f(qr[i2]), E::to_f(cosr[j]), E::to_f(sinr[j]), a, c);
-        y1 = E::from_f(a);
-        y2 = E::from_f(c);
-      } else {
-        y1 = qr[i1];
-        y2 = qr[i2];
-      }
-    }
-    qs[g * kQStride + i1] = y1;
-    qs[g * kQStride + i2] = y2;
-  }
-  const size_t slot = (((size_t)b * p.Hkv + kh) * p.M + past) * kD;
-  if (has_new) {
-    // the append: rotated new key row and raw value row into slot `past`
-    const T* kn = static_cast<const T*>(p.knew) + ((size_t)b * p.Hkv + kh) * kD;
-    const T* vn = static_cast<const T*>(p.vnew) + ((size_t)b * p.Hkv + kh) * kD;
-    T* kb = static_cast<T*>(p.kbuf) + slot;
-    T* vb = static_cast<T*>(p.vbuf) + slot;
-    if (tid < kD / 2) {
-      const int j = tid;
-      const int i1 = p.interleaved ? 2 * j : j;
-      const int i2 = p.interleaved ? 2 * j + 1 : j + kD / 2;
-      T y1 = kn[i1], y2 = kn[i2];
-      if (rot) {
-        float a, c;
-        rotate_pair(E::to_f(kn[i1]), E::to_f(kn[i2]), E::to_f(cosr[j]), E::to_f(sinr[j]), a, c);
-        y1 = E::from_f(a);
-        y2 = E::from_f(c);
-      }
-      news[i1] = y1;
-      news[i2] = y2;
-      kb[i1] = y1;
-      kb[i2] = y2;
-    } else {
-      const int d = (tid - kD / 2) * 2;
-      const T v0 = vn[d], v1 = vn[d + 1];
-      news[kD + d] = v0;
-      news[kD + d + 1] = v1;
-      vb[d] = v0;
-      vb[d + 1] = v1;
-    }
-  }
-  named_bar_sync(1, kCW * 32);
-
-  // query A-fragments: 8 k-steps of 16 dims
-  uint32_t qa[8][4];
-  {
-    const int mi = lane >> 3, r = ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int c = 2 * ks + (mi >> 1);
-      ldsm_x4(smem_u32(qs + r * kQStride + c * 8), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
-    }
-  }
-
   const int gq = lane >> 2, tq = lane & 3;  // fragment row / column group
-  const T* brow0 = nullptr;
-  const T* brow1 = nullptr;
-  if (p.bias) {
-    const int bb = p.bias_b > 1 ? b : 0;
-    const T* bbase = static_cast<const T*>(p.bias) + (size_t)bb * p.bias_h * p.total;
-    const int h0 = kh * G + gq, h1 = kh * G + gq + 8;
-    if (gq < G) brow0 = bbase + (size_t)(p.bias_h > 1 ? h0 : 0) * p.total;
-    if (gq + 8 < G) brow1 = bbase + (size_t)(p.bias_h > 1 ? h1 : 0) * p.total;
-  }
-
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  bool ok = true;
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kStages;
-    if (!mbar_wait(bar_full + 8 * st, (t / kStages) & 1, p.err)) {
-      ok = false;
-      break;
+  const bool rot = p.cos != nullptr;
+  const bool inter = p.interleaved != 0;
+  uint8_t* stage = smem + lay.stage_off;  // raw rows of the next segment (cp.async)
+  T* st_q = reinterpret_cast<T*>(stage);                       // [8*NT][128]
+  T* st_cos = reinterpret_cast<T*>(stage + NT * 8 * 256);      // [64]
+  T* st_sin = st_cos + 64;                                     // [64]
+  T* st_kn = st_sin + 64;                                      // [128]
+  T* st_vn = st_kn + kD;                                       // [128]
+  // Fetch the raw query rows, cos/sin rows and (when the segment holds the
+  // item's last tile) the new K/V rows of a segment into the staging area, as
+  // 16-byte asynchronous copies, so that their latency hides behind the
+  // previous segment's tiles.
+  auto prefetch = [&](int pb, int pkh, int ppast, bool pnew) {
+    const T* qg = static_cast<const T*>(p.q) + ((size_t)pb * p.H + (size_t)pkh * G) * kD;
+    for (int u = tid; u < G * 16; u += kCW * 32) cp_async16(st_q + u * 8, qg + u * 8);
+    if (rot && tid < 16) {
+      const T* src = static_cast<const T*>(tid < 8 ? p.cos : p.sin) + (size_t)ppast * (kD / 2) + (tid & 7) * 8;
+      cp_async16((tid < 8 ? st_cos : st_sin) + (tid & 7) * 8, src);
     }
-    const uint32_t kst = sbase + st * kStageBytes;
-    const uint32_t vst = kst + kTileBytes;
-    const int tk0 = k0 + t * kTile;  // first key of the tile
-    const int wr0 = warp * 16;       // first tile row of this warp
-    bool touched = false;
-    if (has_new && t == ntiles - 1) {
-      const int r = past - tk0;
-      if ((r >> 4) == warp) {
-        const int c = lane & 15;
-        const uint4 val = *reinterpret_cast<const uint4*>(news + (lane < 16 ? 0 : kD) + c * 8);
-        *reinterpret_cast<uint4*>(smem + ((lane < 16 ? kst : vst) - sbase + sw_off(r, c))) = val;
+    if (pnew && tid >= 32 && tid < 64) {
+      const int u = tid - 32;
+      const size_t row = ((size_t)pb * p.Hkv + pkh) * kD;
+      if (u < 16)
+        cp_async16(st_kn + u * 8, static_cast<const T*>(p.knew) + row + u * 8);
+      else
+        cp_async16(st_vn + (u - 16) * 8, static_cast<const T*>(p.vnew) + row + (u - 16) * 8);
+    }
+    cp_async_commit();
+  };
+  long long x = lo_c;
+  int gt = 0;  // tiles consumed by this CTA
+  bool ok = true;
+  prefetch(b, kh, L - 1, istart + tb <= hi_c);
+  while (x < hi_c) {
+    const long long iend = istart + tb;
+    const long long send = iend < hi_c ? iend : hi_c;
+    const int t0 = (int)(x - istart), t1 = (int)(send - istart);
+    const int past = L - 1;
+    const bool has_new = (t1 == tb);  // the item's last tile (holding key `past`) is here
+    const bool splitp = (L - klo) <= 256;  // short items: keep P at fp32-level accuracy
+    // the next segment (if any) always starts the next item
+    int nb = b, nkh = kh, nklo = klo, nL = L, ntb = tb;
+    const bool has_next = send < hi_c;
+    if (has_next) {
+      if (++nkh == p.Hkv) {
+        nkh = 0;
+        do {
+          ++nb;
+          ntb = seq_tiles(p, sl, nb, nklo, nL);
+        } while (ntb == 0);
+      }
+    }
+
+    // -- query rows of the group rotated at position `past` (rows >= G are
+    //    zero), from the staging area
+    cp_async_wait_all();
+    named_bar_sync(1, kCW * 32);  // staging complete; the previous segment's merge reads are done
+    {
+      using V8 = VecT<T, 8>;
+      const int g = tid >> 3, j0 = (tid & 7) * 8;
+      auto rotate8 = [&](const T* src, V8& y1, V8& y2) {
+        V8 x1, x2;
+        if (!inter) {
+          x1 = *reinterpret_cast<const V8*>(src + j0);
+          x2 = *reinterpret_cast<const V8*>(src + kD / 2 + j0);
+        } else {
+          const V8 xa = *reinterpret_cast<const V8*>(src + 2 * j0);
+          const V8 xb = *reinterpret_cast<const V8*>(src + 2 * j0 + 8);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x1.v[e] = xa.v[2 * e];
+            x2.v[e] = xa.v[2 * e + 1];
+            x1.v[e + 4] = xb.v[2 * e];
+            x2.v[e + 4] = xb.v[2 * e + 1];
+          }
+        }
+        if (rot) {
+          const V8 cv = *reinterpret_cast<const V8*>(st_cos + j0);
+          const V8 sv = *reinterpret_cast<const V8*>(st_sin + j0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float a, cc;
+            rotate_pair(E::to_f(x1.v[e]), E::to_f(x2.v[e]), E::to_f(cv.v[e]), E::to_f(sv.v[e]), a, cc);
+            y1.v[e] = E::from_f(a);
+            y2.v[e] = E::from_f(cc);
+          }
+        } else {
+          y1 = x1;
+          y2 = x2;
+        }
+      };
+      auto store8 = [&](T* dst, const V8& y1, const V8& y2) {
+        if (!inter) {
+          *reinterpret_cast<V8*>(dst + j0) = y1;
+          *reinterpret_cast<V8*>(dst + kD / 2 + j0) = y2;
+        } else {
+          V8 ya, yb;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ya.v[2 * e] = y1.v[e];
+            ya.v[2 * e + 1] = y2.v[e];
+            yb.v[2 * e] = y1.v[e + 4];
+            yb.v[2 * e + 1] = y2.v[e + 4];
+          }
+          *reinterpret_cast<V8*>(dst + 2 * j0) = ya;
+          *reinterpret_cast<V8*>(dst + 2 * j0 + 8) = yb;
+        }
+      };
+      for (int gg = g; gg < 8 * NT; gg += 16) {
+        V8 y1, y2;
+        if (gg < G) {
+          rotate8(st_q + gg * kD, y1, y2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y1.v[e] = y2.v[e] = E::from_f(0.f);
+        }
+        store8(qs + gg * kQStride, y1, y2);
+      }
+      if (has_new) {
+        // the append: rotated new key row and raw value row into slot `past`
+        const size_t slot = (((size_t)b * p.Hkv + kh) * p.M + past) * kD;
+        if (tid < 8) {
+          V8 k1, k2;
+          rotate8(st_kn, k1, k2);
+          store8(news, k1, k2);
+          store8(static_cast<T*>(p.kbuf) + slot, k1, k2);
+        } else if (tid < 24) {
+          const int d = (tid - 8) * 8;
+          const V8 vv = *reinterpret_cast<const V8*>(st_vn + d);
+          *reinterpret_cast<V8*>(news + kD + d) = vv;
+          *reinterpret_cast<V8*>(static_cast<T*>(p.vbuf) + slot + d) = vv;
+        }
+      }
+    }
+    named_bar_sync(1, kCW * 32);  // rotated rows ready; the staging area is free
+    if (has_next) prefetch(nb, nkh, nL - 1, iend + ntb <= hi_c);
+
+    // bias rows of this thread's heads (8*nt + 2*tq + e)
+    const T* brow[NT][2];
+    {
+      const int bb = p.bias_b > 1 ? b : 0;
+      const T* bbase = p.bias ? static_cast<const T*>(p.bias) + (size_t)bb * p.bias_h * p.total : nullptr;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hd = 8 * nt + 2 * tq + e;
+          brow[nt][e] = (bbase && hd < G) ? bbase + (size_t)(p.bias_h > 1 ? kh * G + hd : 0) * p.total : nullptr;
+        }
+    }
+    // query B-fragments (d x heads), kept in registers for the whole segment
+    uint32_t qb[NT][8][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t qrow = smem_u32(qs + (8 * nt + (lane & 7)) * kQStride);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ldsm_x4(qrow + (4 * j + (lane >> 3)) * 16, qb[nt][2 * j][0], qb[nt][2 * j][1], qb[nt][2 * j + 1][0],
+                qb[nt][2 * j + 1][1]);
+    }
+
+    // O^T accumulators: d-tile md (rows d = 16 md + gq, +8) x heads (2 tq, 2 tq + 1)
+    float o[NT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+    float mh[NT][2], lh[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mh[nt][0] = mh[nt][1] = -INFINITY, lh[nt][0] = lh[nt][1] = 0.f;
+
+    for (int t = t0; t < t1; ++t, ++gt) {
+      const int st = gt % kStages;
+      if (!mbar_wait(bar_full + 8 * st, (gt / kStages) & 1, p.err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kst = sbase + st * kStageBytes;
+      const uint32_t vst = kst + kTileBytes;
+      const int tk0 = klo + t * kTile;  // first key of the tile
+      const int wr0 = warp * 16;        // first tile row of this warp
+      bool touched = false;
+      if (has_new && t == tb - 1) {
+        const int r = past - tk0;
+        if ((r >> 4) == warp) {
+          const int cch = lane & 15;
+          const uint4 val = *reinterpret_cast<const uint4*>(news + (lane < 16 ? 0 : kD) + cch * 8);
+          *reinterpret_cast<uint4*>(smem + ((lane < 16 ? kst : vst) - sbase + sw_off(r, cch))) = val;
+          touched = true;
+        }
+      }
+      if (tk0 + wr0 + 16 > L) {
+        // value rows beyond the length: zero them, so that P = 0 meets finite V
+        const int rz = max(L - tk0, wr0);
+        const int n = (wr0 + 16 - rz) * 16;
+        for (int idx = lane; idx < n; idx += 32)
+          *reinterpret_cast<uint4*>(smem + (vst - sbase) + sw_off(rz + (idx >> 4), idx & 15)) =
+              make_uint4(0, 0, 0, 0);
         touched = true;
       }
-    }
-    if (tk0 + wr0 + 16 > k1) {
-      // value rows beyond the length: zero them, so that P = 0 meets finite V
-      const int rz = max(k1 - tk0, wr0);
-      const int n = (wr0 + 16 - rz) * 16;
-      for (int idx = lane; idx < n; idx += 32)
-        *reinterpret_cast<uint4*>(smem + (vst - sbase) + sw_off(rz + (idx >> 4), idx & 15)) = make_uint4(0, 0, 0, 0);
-      touched = true;
-    }
-    __syncwarp();
+      __syncwarp();
 
-    // S = Q K^T over this warp's 16 keys
-    float sc[2][4];
+      // S^T = K Q^T: 16 keys (rows) x 8 heads (columns) per n-tile
+      float sc[NT][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-    {
-      const int mi = lane >> 3;
-      const int r = wr0 + ((mi >> 1) << 3) + (lane & 7);
+      for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      {
+        const int mi = lane >> 3;
+        const int kr = wr0 + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kst + sw_off(r, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-        mma_16816<kBF16>(sc[0], qa[ks], b0, b1);
-        mma_16816<kBF16>(sc[1], qa[ks], b2, b3);
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(kst + sw_off(kr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816<kBF16>(sc[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+        }
+      }
+      // scale, bias, mask; the thread's keys are gq and gq + 8 of the warp's 16
+      const int key0 = tk0 + wr0 + gq;
+      uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = key0 + (e >> 1) * 8;
+          float v = sc[nt][e] * p.scale_log2;
+          const T* br = brow[nt][e & 1];
+          if (br && key < L) v = fmaf(E::to_f(br[key]), kLog2e, v);
+          sc[nt][e] = key < L ? v : -INFINITY;
+        }
+        float mx[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float m = fmaxf(sc[nt][e], sc[nt][e + 2]);
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          const float mn = fmaxf(mh[nt][e], m);
+          const float mu = mn == -INFINITY ? 0.f : mn;
+          mx[e] = mu;
+          const float corr = fast_exp2(mh[nt][e] - mu);
+          mh[nt][e] = mn;
+          lh[nt][e] *= corr;
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            o[nt][md][e] *= corr;
+            o[nt][md][e + 2] *= corr;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = fast_exp2(sc[nt][e] - mx[e & 1]);
+        lh[nt][0] += sc[nt][0] + sc[nt][2];
+        lh[nt][1] += sc[nt][1] + sc[nt][3];
+        // P^T (keys x heads) -> B fragments: transpose the two 8x8 halves.
+        // Short items also carry P's rounding residue (P = hi + lo, both
+        // 16-bit), so that P.V keeps fp32-level accuracy where a few keys
+        // dominate the output.
+        const uint32_t h0 = E::pack2(sc[nt][0], sc[nt][1]);
+        const uint32_t h1 = E::pack2(sc[nt][2], sc[nt][3]);
+        bh[nt][0] = movmatrix_trans(h0);
+        bh[nt][1] = movmatrix_trans(h1);
+        if (splitp) {
+          const float2 f0 = E::unpack2(h0), f1 = E::unpack2(h1);
+          bl[nt][0] = movmatrix_trans(E::pack2(sc[nt][0] - f0.x, sc[nt][1] - f0.y));
+          bl[nt][1] = movmatrix_trans(E::pack2(sc[nt][2] - f1.x, sc[nt][3] - f1.y));
+        }
+      }
+      // O^T += V^T P^T over this warp's 16 keys
+      {
+        const int mi = lane >> 3;
+        const int vr = wr0 + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          uint32_t a[4];
+          ldsm_x4_t(vst + sw_off(vr, 2 * md + (mi & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_16816<kBF16>(o[nt][md], a, bh[nt][0], bh[nt][1]);
+            if (splitp) mma_16816<kBF16>(o[nt][md], a, bl[nt][0], bl[nt][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (touched) fence_proxy_async_smem();
+        mbar_arrive(bar_empty + 8 * st);
       }
     }
-    // scale, bias, mask (keys beyond the split end or the true length)
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = tk0 + wr0 + nt * 8 + 2 * tq + (e & 1);
-        float v = sc[nt][e] * p.scale_log2;
-        const T* br = (e < 2) ? brow0 : brow1;
-        if (br && key < k1) v = fmaf(E::to_f(br[key]), kLog2e, v);
-        v = key < k1 ? v : -INFINITY;
-        sc[nt][e] = v;
-        if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
-      }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float c0 = fast_exp2(m0 - mu0), c1 = fast_exp2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      sc[nt][0] = fast_exp2(sc[nt][0] - mu0);
-      sc[nt][1] = fast_exp2(sc[nt][1] - mu0);
-      sc[nt][2] = fast_exp2(sc[nt][2] - mu1);
-      sc[nt][3] = fast_exp2(sc[nt][3] - mu1);
-      ps0 += sc[nt][0] + sc[nt][1];
-      ps1 += sc[nt][2] + sc[nt][3];
-    }
-    l0 = l0 * c0 + ps0;
-    l1 = l1 * c1 + ps1;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= c0;
-      o[i][1] *= c0;
-      o[i][2] *= c1;
-      o[i][3] *= c1;
-    }
-    uint32_t pa[4];
-    pa[0] = E::pack2(sc[0][0], sc[0][1]);
-    pa[1] = E::pack2(sc[0][2], sc[0][3]);
-    pa[2] = E::pack2(sc[1][0], sc[1][1]);
-    pa[3] = E::pack2(sc[1][2], sc[1][3]);
-    // O += P V
-    {
-      const int mi = lane >> 3;
-      const int r = wr0 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-      for (int pp = 0; pp < 8; ++pp) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vst + sw_off(r, 2 * pp + (mi >> 1)), b0, b1, b2, b3);
-        mma_16816<kBF16>(o[2 * pp], pa, b0, b1);
-        mma_16816<kBF16>(o[2 * pp + 1], pa, b2, b3);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      if (touched) fence_proxy_async_smem();
-      mbar_arrive(bar_empty + 8 * st);
-    }
-  }
 
-  // ---------------- merge the four warps ----------------
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  // every warp is done reading the ring; leave together if any wait ran out
-  if (!named_bar_and(1, kCW * 32, ok)) return;
-  float* sm_o = reinterpret_cast<float*>(smem);               // [kCW][16][kD]
-  float* sm_ml = reinterpret_cast<float*>(smem) + kCW * 16 * kD;  // [kCW][16][2]
-  {
-    float* wo = sm_o + warp * 16 * kD;
+    // -- merge the four warps' (O^T, m, l) in two rounds through shared memory
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int d = i * 8 + 2 * tq;
-      if (gq < G) *reinterpret_cast<float2*>(wo + gq * kD + d) = make_float2(o[i][0], o[i][1]);
-      if (gq + 8 < G) *reinterpret_cast<float2*>(wo + (gq + 8) * kD + d) = make_float2(o[i][2], o[i][3]);
-    }
-    if (tq == 0) {
-      float* wml = sm_ml + warp * 32;
-      wml[2 * gq] = m0;
-      wml[2 * gq + 1] = l0;
-      wml[2 * (gq + 8)] = m1;
-      wml[2 * (gq + 8) + 1] = l1;
-    }
-  }
-  named_bar_sync(1, kCW * 32);
-  T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
-  for (int u = tid; u < G * kD; u += kCW * 32) {
-    const int g = u / kD, d = u % kD;
-    float ms = -INFINITY;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int w = 0; w < kCW; ++w) ms = fmaxf(ms, sm_ml[w * 32 + 2 * g]);
-    float acc = 0.f, l = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCW; ++w) {
-      const float f = fast_exp2(sm_ml[w * 32 + 2 * g] - ms);
-      acc += f * sm_o[(w * 16 + g) * kD + d];
-      l += f * sm_ml[w * 32 + 2 * g + 1];
-    }
-    if (nsplit_b == 1) {
-      outg[(size_t)g * kD + d] = E::from_f(acc / l);
-    } else {
-      const size_t idx = ((size_t)b * p.H + (size_t)kh * G + g) * p.nsplit + s;
-      p.part_o[idx * kD + d] = acc;
-      if (d == 0) {
-        p.part_ml[2 * idx] = ms;
-        p.part_ml[2 * idx + 1] = l;
+      for (int e = 0; e < 2; ++e) {
+        float l = lh[nt][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        lh[nt][e] = l;
       }
+    // every warp is done reading the ring and the query rows; leave together
+    // if any wait ran out
+    if (!named_bar_and(1, kCW * 32, ok)) return;
+    float* mw = reinterpret_cast<float*>(smem + lay.merge_off);
+    const int wfl = lay.merge_warp_bytes / 4;  // floats per hand-off slot
+    auto hand_off = [&](float* dst) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int md = 0; md < 8; ++md)
+          *reinterpret_cast<float4*>(dst + ((nt * 8 + md) * 32 + lane) * 4) =
+              make_float4(o[nt][md][0], o[nt][md][1], o[nt][md][2], o[nt][md][3]);
+        *reinterpret_cast<float4*>(dst + NT * 8 * 128 + (nt * 32 + lane) * 4) =
+            make_float4(mh[nt][0], lh[nt][0], mh[nt][1], lh[nt][1]);
+      }
+    };
+    auto absorb = [&](const float* src) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float4 ml = *reinterpret_cast<const float4*>(src + NT * 8 * 128 + (nt * 32 + lane) * 4);
+        float f1[2], f2[2];
+        const float m2[2] = {ml.x, ml.z}, l2[2] = {ml.y, ml.w};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float ms = fmaxf(mh[nt][e], m2[e]);
+          const float su = ms == -INFINITY ? 0.f : ms;
+          f1[e] = fast_exp2(mh[nt][e] - su);
+          f2[e] = fast_exp2(m2[e] - su);
+          lh[nt][e] = lh[nt][e] * f1[e] + l2[e] * f2[e];
+          mh[nt][e] = ms;
+        }
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          const float4 a = *reinterpret_cast<const float4*>(src + ((nt * 8 + md) * 32 + lane) * 4);
+          o[nt][md][0] = o[nt][md][0] * f1[0] + a.x * f2[0];
+          o[nt][md][1] = o[nt][md][1] * f1[1] + a.y * f2[1];
+          o[nt][md][2] = o[nt][md][2] * f1[0] + a.z * f2[0];
+          o[nt][md][3] = o[nt][md][3] * f1[1] + a.w * f2[1];
+        }
+      }
+    };
+    if (warp >= 2) hand_off(mw + (warp - 2) * wfl);
+    named_bar_sync(1, kCW * 32);
+    if (warp < 2) absorb(mw + warp * wfl);
+    named_bar_sync(1, kCW * 32);
+    if (warp == 1) hand_off(mw);
+    named_bar_sync(1, kCW * 32);
+    if (warp == 0) {
+      absorb(mw);
+      const bool whole = (t0 == 0 && t1 == tb);
+      const int slot = (t0 == 0) ? 1 : 0;  // tail: begins here and runs on; head: began earlier
+      T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
+      float* po = p.part_o + ((size_t)c * 2 + slot) * G * kD;
+      float* pm = p.part_ml + ((size_t)c * 2 + slot) * G * 2;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int hd0 = 8 * nt + 2 * tq;  // this thread's heads: hd0, hd0 + 1
+        const float i0 = 1.f / lh[nt][0], i1 = 1.f / lh[nt][1];
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          const int d = 16 * md + gq;
+          if (whole) {
+            if (hd0 < G) {
+              outg[(size_t)hd0 * kD + d] = E::from_f(o[nt][md][0] * i0);
+              outg[(size_t)hd0 * kD + d + 8] = E::from_f(o[nt][md][2] * i0);
+            }
+            if (hd0 + 1 < G) {
+              outg[(size_t)(hd0 + 1) * kD + d] = E::from_f(o[nt][md][1] * i1);
+              outg[(size_t)(hd0 + 1) * kD + d + 8] = E::from_f(o[nt][md][3] * i1);
+            }
+          } else {
+            if (hd0 < G) {
+              po[(size_t)hd0 * kD + d] = o[nt][md][0];
+              po[(size_t)hd0 * kD + d + 8] = o[nt][md][2];
+            }
+            if (hd0 + 1 < G) {
+              po[(size_t)(hd0 + 1) * kD + d] = o[nt][md][1];
+              po[(size_t)(hd0 + 1) * kD + d + 8] = o[nt][md][3];
+            }
+          }
+        }
+        if (!whole && gq == 0) {
+          if (hd0 < G) *reinterpret_cast<float2*>(pm + 2 * hd0) = make_float2(mh[nt][0], lh[nt][0]);
+          if (hd0 + 1 < G) *reinterpret_cast<float2*>(pm + 2 * (hd0 + 1)) = make_float2(mh[nt][1], lh[nt][1]);
+        }
+      }
+    }
+
+    // -- next segment
+    x = send;
+    if (has_next) {
+      istart = iend;
+      b = nb;
+      kh = nkh;
+      klo = nklo;
+      L = nL;
+      tb = ntb;
     }
   }
 }
 
-struct CombineParams {
-  const int32_t* seqlens;
-  const float* part_o;
-  const float* part_ml;
-  void* out;
-  int H, M, total, window, chunk, nsplit;
-};
+// Merges the partials of every (sequence, KV head) item that was cut by CTA
+// boundaries: with partials (o_i, m_i, l_i) from CTAs c0..c1,
+//   m* = max_i m_i,  o = sum_i 2^(m_i - m*) o_i / sum_i 2^(m_i - m*) l_i.
+// One CTA per item; items finished inside one CTA are skipped.  The lengths
+// are read before waiting for the decode kernel (they are inputs); the
+// partial statistics, then the partial outputs, are each fetched in one
+// batch of independent loads.
+constexpr int kCombineMaxCached = 64;  // partials whose (m, l) are kept in shared memory
 
-// Merges the per-split partials of every (sequence, query head) whose
-// sequence needed more than one split:
-//   m* = max_s m_s,  o = sum_s 2^(m_s - m*) o_s / sum_s 2^(m_s - m*) l_s.
 template <typename T>
-__global__ void __launch_bounds__(kD) combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
   using E = Elem<T>;
-  pdl_wait_primary();
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int past = p.seqlens[b];
-  if (sequence_error(past, 1, p.M, p.total)) return;
-  const int L = past + 1;
-  const int lo = p.window > 0 ? max(0, L - p.window) : 0;
-  const int ns = (L - lo + p.chunk - 1) / p.chunk;
-  if (ns <= 1) return;
-  const size_t base = ((size_t)b * p.H + h) * p.nsplit;
-  const float* ml = p.part_ml + 2 * base;
-  float ms = -INFINITY;
-  for (int i = 0; i < ns; ++i) ms = fmaxf(ms, ml[2 * i]);
-  const int d = threadIdx.x;
-  float acc = 0.f, l = 0.f;
-  for (int i = 0; i < ns; ++i) {
-    const float f = fast_exp2(ml[2 * i] - ms);
-    acc += f * p.part_o[(base + i) * kD + d];
-    l += f * ml[2 * i + 1];
+  __shared__ int s_seq[kSeqCache];
+  __shared__ float s_m[kCombineMaxCached * kDecodeMaxGroup];
+  __shared__ float s_l[kCombineMaxCached * kDecodeMaxGroup];
+  __shared__ float s_ms[kDecodeMaxGroup];
+  const int kh = blockIdx.x, b = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool cached = p.B <= kSeqCache;
+  if (cached)
+    for (int i = tid; i < p.B; i += kD) s_seq[i] = p.seqlens[i];
+  __syncthreads();
+  const int* sl = cached ? s_seq : p.seqlens;
+  int lo, L;
+  const int tb = seq_tiles(p, sl, b, lo, L);
+  if (tb == 0) {
+    // the sequence failed the length check: the decode kernel skipped it
+    if (kh == 0 && tid == 0) record_error(p.err, sequence_error(sl[b], 1, p.M, p.total));
+    return;
   }
-  static_cast<T*>(p.out)[((size_t)b * p.H + h) * kD + d] = E::from_f(acc / l);
+  // global index of the first tile of sequence b's items, and the total
+  long long sstart = 0, Ttot = 0;
+  {
+    long long base = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      int l2, L2;
+      const int bi = b0 + lane;
+      const long long t = (bi < p.B ? seq_tiles(p, sl, bi, l2, L2) : 0) * (long long)p.Hkv;
+      const long long incl = warp_incl_scan_ll(t, lane);
+      const int src = b - b0;
+      if (src >= 0 && src < 32) sstart = base + __shfl_sync(0xffffffffu, incl - t, src);
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    Ttot = base;
+  }
+  const long long start = sstart + (long long)kh * tb;
+  const int c0 = cta_of(start, Ttot, p.P);
+  const int c1 = cta_of(start + tb - 1, Ttot, p.P);
+  if (c0 == c1) return;
+  // CTAs c0..c1 each hold one partial of this item (the tail slot of c0,
+  // the head slot of the others), except CTAs whose tile range is empty
+  // (only when there are fewer tiles than CTAs).
+  const int n = c1 - c0 + 1;
+  const int G = p.G;
+  auto empty = [&](int i) { return Ttot * (c0 + i) / p.P == Ttot * (c0 + i + 1) / p.P; };
+  auto slot_of = [&](int i, int g) { return ((size_t)(c0 + i) * 2 + (i == 0 ? 1 : 0)) * G + g; };
+  pdl_wait_primary();
+
+  // statistics of every (partial, head) pair, one pair per thread
+  for (int u = tid; u < n * G; u += kD) {
+    const int i = u / G, g = u - i * G;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (!empty(i)) ml = *reinterpret_cast<const float2*>(p.part_ml + 2 * slot_of(i, g));
+    if (i < kCombineMaxCached) {
+      s_m[i * kDecodeMaxGroup + g] = ml.x;
+      s_l[i * kDecodeMaxGroup + g] = ml.y;
+    }
+  }
+  __syncthreads();
+  auto stat = [&](int i, int g, float& m, float& l) {
+    if (i < kCombineMaxCached) {
+      m = s_m[i * kDecodeMaxGroup + g];
+      l = s_l[i * kDecodeMaxGroup + g];
+    } else if (empty(i)) {
+      m = -INFINITY;
+      l = 0.f;
+    } else {
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + 2 * slot_of(i, g));
+      m = ml.x;
+      l = ml.y;
+    }
+  };
+  if (tid < G) {
+    float ms = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+      float m, l;
+      stat(i, tid, m, l);
+      ms = fmaxf(ms, m);
+    }
+    s_ms[tid] = ms;
+  }
+  __syncthreads();
+  // outputs: warp w handles heads w, w+4, ...; each lane 4 consecutive dims
+  const int d4 = lane * 4;
+  for (int g = warp; g < G; g += kD / 32) {
+    const float ms = s_ms[g];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
+    for (int i0 = 0; i0 < n; i0 += 4) {
+      float4 ov[4];
+      float wv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k;
+        ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[k] = 0.f;
+        if (i < n && !empty(i)) {
+          ov[k] = *reinterpret_cast<const float4*>(p.part_o + slot_of(i, g) * kD + d4);
+          float m, lk;
+          stat(i, g, m, lk);
+          wv[k] = fast_exp2(m - ms);
+          l += wv[k] * lk;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc.x += wv[k] * ov[k].x;
+        acc.y += wv[k] * ov[k].y;
+        acc.z += wv[k] * ov[k].z;
+        acc.w += wv[k] * ov[k].w;
+      }
+    }
+    const float inv = 1.f / l;
+    T* o = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G + g) * kD + d4;
+    uint2 packed;
+    packed.x = E::pack2(acc.x * inv, acc.y * inv);
+    packed.y = E::pack2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(o) = packed;
+  }
 }
 
 template <typename T>
 cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, float* part_o, float* part_ml) {
-  const CUtensorMapDataType dt = a.dtype == GQA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType dt =
+      a.dtype == GQA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap kmap, vmap;
   const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * a.Hkv * a.M};
   const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
@@ -443,26 +808,27 @@ cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, float* part_o, floa
       !encode_tensor_map(&vmap, dt, 2, a.vbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
 
+  const int G = a.H / a.Hkv;
   DecodeParams p{a.q, a.k, a.v, a.kbuf, a.vbuf, a.seqlens, a.cos, a.sin, a.bias, a.out, part_o, part_ml, a.err,
-                 a.H, a.Hkv, a.H / a.Hkv, a.M, a.total, a.window, plan.chunk, plan.nsplit, a.interleaved,
-                 a.bias_b, a.bias_h, a.scale * kLog2e};
-  auto kern = decode_kernel<T>;
-  static bool attr_set[64] = {};
+                 a.B, a.H, a.Hkv, G, a.M, a.total, a.window, plan.ctas, a.interleaved, a.bias_b, a.bias_h,
+                 a.scale * kLog2e};
+  const int smem = layout_for(G).total;
+  auto kern = G <= 8 ? decode_kernel<T, 1> : decode_kernel<T, 2>;
+  static int attr_set[64][2] = {};  // dynamic shared memory set so far, per device and variant
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const int vi = G <= 8 ? 0 : 1;
+  if (dev < 0 || dev >= 64 || attr_set[dev][vi] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev][vi] = smem;
   }
-  const dim3 grid(plan.nsplit, a.Hkv, a.B);
-  kern<<<grid, kThreads, kSmemBytes, a.stream>>>(kmap, vmap, p);
+  kern<<<plan.ctas, kThreads, smem, a.stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || plan.nsplit <= 1) return e;
+  if (e != cudaSuccess) return e;
 
-  CombineParams cp{a.seqlens, part_o, part_ml, a.out, a.H, a.M, a.total, a.window, plan.chunk, plan.nsplit};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.H, a.B);
+  cfg.gridDim = dim3(a.Hkv, a.B);
   cfg.blockDim = dim3(kD);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = a.stream;
@@ -471,12 +837,16 @@ cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, float* part_o, floa
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel<T>, cp);
+  return cudaLaunchKernelEx(&cfg, combine_kernel<T>, p);
 }
 
 }  // namespace
 
-int decode_smem_bytes() { return kSmemBytes; }
+int decode_ctas_per_sm(int G, int smem_per_sm) {
+  const size_t per = (size_t)layout_for(G).total + kSmReservedPerCta;
+  const int n = (int)((smem_per_sm > 0 ? (size_t)smem_per_sm : kSmPerSM) / per);
+  return n < 1 ? 1 : (n > 2 ? 2 : n);
+}
 
 cudaError_t launch_decode(const ForwardArgs& a, const Plan& plan, float* part_o, float* part_ml) {
   return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, plan, part_o, part_ml)

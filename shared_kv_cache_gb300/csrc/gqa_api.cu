@@ -74,6 +74,19 @@ gqa_status_t check_dims(const gqa_dims_t* d) {
   return GQA_OK;
 }
 
+int smem_per_sm() {
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 233472;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || n <= 0)
+      return 233472;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 }  // namespace
 
 // Accessors for other translation units of the library.
@@ -84,28 +97,19 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
   Plan pl{};
   const int G = H / Hkv;
   if (S == 1 && D == 128 && G <= kDecodeMaxGroup) {
+    // Persistent split-KV decode: P CTAs, each leaving at most two partials.
     pl.path = Path::kDecode;
-    const long long leff = window > 0 ? std::min(total, window) : total;
-    // Aim for about four waves of two CTAs per SM when sequences are on
-    // average half the longest length; chunks are whole tiles.
-    const long long est_rows = (long long)B * Hkv * leff / 2;
-    const long long target = 8LL * num_sms;
-    long long chunk = (est_rows + target - 1) / target;
-    chunk = (chunk + kDecodeTile - 1) / kDecodeTile * kDecodeTile;
-    chunk = std::max<long long>(kDecodeTile, std::min<long long>(chunk, 4096));
-    pl.chunk = (int)chunk;
-    pl.nsplit = (int)((leff + chunk - 1) / chunk);
-    if (pl.nsplit < 1) pl.nsplit = 1;
+    pl.ctas = num_sms * decode_ctas_per_sm(G, smem_per_sm());
     size_t off = 0;
-    if (pl.nsplit > 1) {
-      pl.part_o_off = off;
-      pl.part_o_bytes = (size_t)B * H * pl.nsplit * D * sizeof(float);
-      off = align_up(off + pl.part_o_bytes, 256);
-      pl.part_ml_off = off;
-      pl.part_ml_bytes = (size_t)B * H * pl.nsplit * 2 * sizeof(float);
-      off = align_up(off + pl.part_ml_bytes, 256);
-    }
+    pl.part_o_off = off;
+    pl.part_o_bytes = (size_t)pl.ctas * 2 * G * D * sizeof(float);
+    off = align_up(off + pl.part_o_bytes, 256);
+    pl.part_ml_off = off;
+    pl.part_ml_bytes = (size_t)pl.ctas * 2 * G * 2 * sizeof(float);
+    off = align_up(off + pl.part_ml_bytes, 256);
     pl.total_bytes = off;
+    (void)total;
+    (void)window;
     return pl;
   }
   pl.path = Path::kGeneric;

@@ -40,11 +40,10 @@ enum class Path { kDecode, kPrefillTC, kGeneric };
 // dims alone, so gqa_workspace_size() and gqa_forward() agree.
 struct Plan {
   Path path;
-  int chunk = 0;   // decode: keys per split (multiple of the tile)
-  int nsplit = 0;  // decode: splits per (sequence, KV head) at the longest length
+  int ctas = 0;    // decode: persistent grid size P
   size_t q_rot_off = 0, q_rot_bytes = 0;    // rotated queries, T [B, S, H, D]
-  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [B, H, nsplit, D]
-  size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [B, H, nsplit, 2]
+  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [P, 2, G, D]
+  size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [P, 2, G, 2]
   size_t total_bytes = 0;
 };
 
@@ -58,6 +57,7 @@ int device_sm_count();
 cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot);
 cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src);
 cudaError_t launch_decode(const ForwardArgs& a, const Plan& plan, float* part_o, float* part_ml);
+int decode_ctas_per_sm(int group, int smem_per_sm);  // resident decode CTAs per SM (1 or 2)
 cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).

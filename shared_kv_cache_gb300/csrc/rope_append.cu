@@ -16,11 +16,6 @@
 namespace gqa {
 namespace {
 
-template <typename T, int N>
-struct alignas(sizeof(T) * N) VecT {
-  T v[N];
-};
-
 struct RopeParams {
   const void* q;
   const void* k;

@@ -121,6 +121,9 @@ def test_chunked_overflow_is_an_error_and_writes_nothing():
     dict(rotary=False, seed=17),
     dict(interleaved=1, seed=18),
     dict(M=4096, past=(4095, 3000, 17), total=4096, seed=19),   # the last slot of the buffer
+    # many short items and a few long ones: CTAs see many segments each
+    dict(B=40, H=16, Hkv=4, M=3000, past=tuple([0, 1, 2, 63, 64, 65] * 6 + [2999, 1500, 777, 128]), seed=22),
+    dict(B=40, H=16, Hkv=4, M=3000, past=tuple([5] * 39 + [2999]), window=700, seed=23),
 ])
 def test_decode_cases(kw):
     check(custom(**kw))

@@ -114,9 +114,11 @@ def test_workspace_checks(lib):
 
 
 def test_workspace_plan_decode(lib):
-    # decode at D = 128 uses split-KV partials; one split needs no scratch
+    # decode at D = 128: at most two fp32 partials (G x (D + 2) floats) per
+    # persistent CTA, whatever the lengths
     d = dims(seq_len=1, head_size=128, num_heads=32, kv_num_heads=8, batch=16, max_seq_len=4096)
     big = gqa.gqa_workspace_size(d, 4096, 0)
     assert big > 0 and big % 256 == 0
-    d1 = dims(seq_len=1, head_size=128, num_heads=4, kv_num_heads=4, batch=1, max_seq_len=64)
-    assert gqa.gqa_workspace_size(d1, 33, 0) == 0
+    assert gqa.gqa_workspace_size(d, 17, 0) == big == gqa.gqa_workspace_size(d, 4096, 100)
+    per_cta = 2 * 4 * 130 * 4
+    assert big >= 152 * per_cta and big <= 2 * 152 * per_cta + 512

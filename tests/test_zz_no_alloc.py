@@ -1,7 +1,7 @@
 """gqa_decode_noalloc: the decode step for callers that cannot allocate device
 memory when they run it (a runtime whose memory planner hands out every
 buffer ahead of execution, a serving loop where cudaMalloc/cudaFree may not
-synchronise the device).  Its scratch is a static 16 MiB device array inside
+synchronise the device).  Its scratch is a static 4 MiB device array inside
 the library instead of a caller-supplied workspace.
 
 The GPU test calls it twice in a row through the C ABI and checks each
@@ -16,7 +16,7 @@ from shared_kv_cache_gb300 import workloads as W
 
 from gqa_cases import TOL, run_cuda, to_device
 
-STATIC_SCRATCH_BYTES = 16 << 20
+STATIC_SCRATCH_BYTES = 4 << 20
 
 
 def _dims(w, inp):
@@ -55,19 +55,21 @@ def test_noalloc_matches_gqa_forward_on_two_calls(name):
         assert np.array_equal(W.bits(d["v_buf"].cpu()), W.bits(ref_vb))
 
 
-def test_noalloc_rejects_calls_beyond_the_static_scratch():
-    """64 sequences x 64 heads over 32768 slots need more partials than the
-    static array holds: rejected before any launch (the pointers below are
-    never dereferenced)."""
+def test_noalloc_scratch_bound_and_rejected_shapes():
+    """The decode kernels need at most two partials of G x (128 + 2) floats
+    per persistent CTA, whatever the lengths, so the largest decode shape fits
+    the static array; shapes other than the decode shape are rejected before
+    any launch (the pointers below are never dereferenced)."""
     gqa.load_library()
-    d = gqa.make_dims(64, 1, 64, 8, 128, 32768, "bf16", 0, 32768, 1, 1)
-    assert gqa.gqa_workspace_size(d, 32768, 0) > STATIC_SCRATCH_BYTES
+    for G in (1, 4, 8, 16):
+        d = gqa.make_dims(64, 1, 8 * G, 8, 128, 32768, "bf16", 0, 32768, 1, 1)
+        assert gqa.gqa_workspace_size(d, 32768, 0) <= STATIC_SCRATCH_BYTES
     p = [0x100000 * (i + 1) for i in range(12)]
-    st = gqa.gqa_decode_noalloc(d, p[0], p[1], p[2], p[3], p[4], p[3], p[4], p[5], 32768, p[6], p[7], 0.0, 0,
+    d2 = gqa.make_dims(2, 4, 8, 2, 128, 256, "fp16", 0, 256, 1, 1)   # four new tokens: not a decode step
+    st = gqa.gqa_decode_noalloc(d2, p[0], p[1], p[2], p[3], p[4], p[3], p[4], p[5], 64, p[6], p[7], 0.0, 0,
                                 None, p[8], None)
     assert st == gqa.GQA_ERR_UNSUPPORTED
-    # shapes other than the decode shape are not served by this entry point either
-    d2 = gqa.make_dims(2, 4, 8, 2, 128, 256, "fp16", 0, 256, 1, 1)
-    st = gqa.gqa_decode_noalloc(d2, p[0], p[1], p[2], p[3], p[4], p[3], p[4], p[5], 64, p[6], p[7], 0.0, 0,
+    d3 = gqa.make_dims(2, 1, 8, 2, 64, 256, "fp16", 0, 256, 1, 1)    # head size 64
+    st = gqa.gqa_decode_noalloc(d3, p[0], p[1], p[2], p[3], p[4], p[3], p[4], p[5], 64, p[6], p[7], 0.0, 0,
                                 None, p[8], None)
     assert st == gqa.GQA_ERR_UNSUPPORTED
