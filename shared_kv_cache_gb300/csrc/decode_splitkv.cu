@@ -437,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     for (int t = t0; t < t1; ++t, ++gt) {
       const int st = gt % kStages;
-      if (!mbar_wait(bar_full + 8 * st, (gt / kStages) & 1, p.err)) {
-        ok = false;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (gt / kStages) & 1, p.err))) {
+        ok = false;  // the whole warp leaves together
         break;
       }
       const uint32_t kst = sbase + st * kStageBytes;

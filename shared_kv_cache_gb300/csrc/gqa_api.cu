@@ -112,7 +112,7 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
     (void)window;
     return pl;
   }
-  pl.path = Path::kGeneric;
+  pl.path = (S > 1 && D == 128) ? Path::kPrefillTC : Path::kGeneric;
   if (rotary) {
     pl.q_rot_off = 0;
     pl.q_rot_bytes = (size_t)B * S * H * D * 2;
@@ -240,7 +240,9 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
     case Path::kGeneric: {
       void* q_rot = cos_cache ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
       e = launch_rope_append(a, q_rot);
-      if (e == cudaSuccess) e = launch_attn_generic(a, q_rot ? q_rot : query);
+      if (e == cudaSuccess)
+        e = pl.path == Path::kPrefillTC ? launch_prefill_tc(a, q_rot ? q_rot : query)
+                                        : launch_attn_generic(a, q_rot ? q_rot : query);
       break;
     }
   }

@@ -1,0 +1,423 @@
+// Prefill attention on the 5th-generation tensor cores (tcgen05 + TMEM),
+// head size 128, for S > 1 new tokens per sequence.
+//
+// What it computes ("KV Cache", rocMLIR discussion, "Example": gemm0 = Q x K,
+// softmax, gemm1 = QK x V; the causal mask k_pos <= past_len + q_pos of
+// "[TorchOnnxToTorch] Add pad+scatter KV cache and mask to GQA"; the additive
+// attention_bias and the sliding window of "Clarification about
+// GroupQueryAttention behavior"): for every new token i of sequence b and
+// query head h, over the keys of KV head h / (H / Hkv) at positions
+// j <= p = past_b + i (and j > p - W with a window W), the softmax of the
+// scaled scores (plus bias) weighting the value rows.  The key scan of a query
+// tile stops at the last key its rows can see; it never sweeps max_seq_len.
+//
+// One CTA per (sequence, query head, tile of 128 new tokens).  Warp roles:
+//   warp 0      bulk-tensor (TMA) loads: the query tile once, then the K and V
+//               tiles of 128 keys through two 2-stage rings;
+//   warp 1      owns TMEM; lane 0 issues the MMAs:
+//                 S_j = Q K_j^T            (A, B from shared memory)
+//                 O  += P_j V_j            (A = P_j from TMEM, B = V_j MN-major)
+//               S_{j+1} is issued before P_j V_j, so the tensor core computes
+//               the next scores while the softmax warps work on tile j;
+//   warps 2..5  softmax: thread r owns query row r (TMEM lane r), reads its
+//               128 scores, applies scale, bias and mask, updates the running
+//               max and sum, writes P_j (16-bit) over S_j in TMEM, and rescales
+//               O in TMEM only when the row max grew by more than 2^8 (the
+//               un-rescaled terms stay bounded by 2^8 and the final division
+//               uses the same reference max); finally O / l goes to the output.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O [256,384) of a 512-column
+// allocation (one CTA per SM: the shared-memory footprint sees to that).
+#include "common.cuh"
+#include "internal.h"
+#include "tc.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBM = 128;   // query rows per tile
+constexpr int kBN = 128;   // keys per KV tile
+constexpr int kKSt = 2;    // K ring stages
+constexpr int kVSt = 2;    // V ring stages
+constexpr int kThreads = 192;
+constexpr int kTileBytes = kBN * kD * 2;       // 32 KB: two 128-row x 128-byte boxes
+constexpr int kBoxBytes = kTileBytes / 2;
+constexpr int kQOff = 0;
+constexpr int kKOff = kQOff + kBM * kD * 2;
+constexpr int kVOff = kKOff + kKSt * kTileBytes;
+constexpr int kBarOff = kVOff + kVSt * kTileBytes;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, drain
+constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 1 + 1;
+constexpr int kSlotOff = kBarOff + kNumBars * 8;
+constexpr int kSmemBytes = kSlotOff + 16 + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThresh = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
+
+struct PrefillParams {
+  int* err;
+  const int32_t* seqlens;
+  const void* bias;  // [Bb, Hb, S, total] or nullptr
+  void* out;         // [B, S, H*D]
+  int B, S, H, Hkv, M, total, window, bias_b, bias_h, n_qt;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  using E = Elem<T>;
+  constexpr bool kBF16 = E::is_bf16;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar0 = sb + kBarOff;
+  const uint32_t q_full = bar0;
+  const uint32_t k_full = bar0 + 8, k_empty = k_full + 8 * kKSt;
+  const uint32_t v_full = k_empty + 8 * kKSt, v_empty = v_full + 8 * kVSt;
+  const uint32_t s_full = v_empty + 8 * kVSt, p_full = s_full + 16;
+  const uint32_t o_done = p_full + 16, drain = o_done + 8;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // work item: heaviest query tiles first
+  const int bh = blockIdx.x % (p.B * p.H);
+  const int qt = p.n_qt - 1 - blockIdx.x / (p.B * p.H);
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int kh = h / (p.H / p.Hkv);
+  const int past = p.seqlens[b];
+  if (sequence_error(past, p.S, p.M, p.total)) return;  // recorded by the append kernel
+  const int i0 = qt * kBM;
+  const int i1 = min(i0 + kBM, p.S);
+  const int L = past + p.S;
+  const int kstart = p.window > 0 ? max(0, past + i0 - p.window + 1) : 0;
+  const int kend = past + i1;  // one past the last key any row of the tile sees
+  const int n_kv = (kend - kstart + kBN - 1) / kBN;
+  // bf16 tiles whose first row sees few keys also carry P's rounding residue
+  // (P = hi + lo, both bf16; lo in the upper 64 columns of the S buffer) so
+  // that P.V keeps fp32-level accuracy where a few keys dominate the output
+  const int min_keys = p.window > 0 ? min(p.window, past + i0 + 1) : past + i0 + 1;
+  const bool splitp = kBF16 && min_keys <= 256;
+
+  if (tid == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kKSt; ++s) {
+      mbar_init(k_full + 8 * s, 1);
+      mbar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < kVSt; ++s) {
+      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(s_full + 8 * s, 1);
+      mbar_init(p_full + 8 * s, 128);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tc::alloc(smem_u32(tslot), kTmemCols);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t tS = tbase, tO = tbase + 256;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&qmap);
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+      mbar_arrive_expect_tx(q_full, kBM * kD * 2);
+      tma_load_4d(sb + kQOff, &qmap, 0, h, i0, b, q_full);
+      tma_load_4d(sb + kQOff + kBoxBytes, &qmap, 64, h, i0, b, q_full);
+      const int zkv = b * p.Hkv + kh;
+      int issued_k = 0, issued_v = 0;
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int y = kstart + j * kBN;
+        const int ks = j % kKSt, vs = j % kVSt;
+        if (j >= kKSt && !mbar_wait(k_empty + 8 * ks, ((j / kKSt) - 1) & 1, p.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(k_full + 8 * ks, kTileBytes);
+        tma_load_3d(sb + kKOff + ks * kTileBytes, &kmap, 0, y, zkv, k_full + 8 * ks);
+        tma_load_3d(sb + kKOff + ks * kTileBytes + kBoxBytes, &kmap, 64, y, zkv, k_full + 8 * ks);
+        issued_k = j + 1;
+        if (j >= kVSt && !mbar_wait(v_empty + 8 * vs, ((j / kVSt) - 1) & 1, p.err)) { ok = false; break; }
+        mbar_arrive_expect_tx(v_full + 8 * vs, kTileBytes);
+        tma_load_3d(sb + kVOff + vs * kTileBytes, &vmap, 0, y, zkv, v_full + 8 * vs);
+        tma_load_3d(sb + kVOff + vs * kTileBytes + kBoxBytes, &vmap, 64, y, zkv, v_full + 8 * vs);
+        issued_v = j + 1;
+      }
+      // no copy may still be in flight into shared memory when the CTA exits
+      mbar_wait(q_full, 0, p.err);
+      for (int j = max(0, issued_k - kKSt); j < issued_k; ++j) mbar_wait(k_full + 8 * (j % kKSt), (j / kKSt) & 1, p.err);
+      for (int j = max(0, issued_v - kVSt); j < issued_v; ++j) mbar_wait(v_full + 8 * (j % kVSt), (j / kVSt) & 1, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t id_s = tc::idesc_f16(kBF16, kBM, kBN, false, false);
+      const uint32_t id_o = tc::idesc_f16(kBF16, kBM, kD, false, true);
+      bool ok = mbar_wait(q_full, 0, p.err);
+      auto issue_s = [&](int j) -> bool {
+        const int ks = j % kKSt;
+        if (!mbar_wait(k_full + 8 * ks, (j / kKSt) & 1, p.err)) return false;
+        tc::fence_after();
+        const uint32_t qa = sb + kQOff, kb = sb + kKOff + ks * kTileBytes;
+        const uint32_t d = tS + (j & 1) * 128;
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
+          tc::mma_ss(d, tc::smem_desc(qa + off, 16, 1024, tc::kSwizzle128B),
+                     tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), id_s, k > 0 ? 1u : 0u);
+        }
+        tc::commit(s_full + 8 * (j & 1));
+        tc::commit(k_empty + 8 * ks);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n_kv && ok; ++j) {
+        if (j + 1 < n_kv && !issue_s(j + 1)) { ok = false; break; }
+        if (!mbar_wait(p_full + 8 * (j & 1), (j >> 1) & 1, p.err)) { ok = false; break; }
+        const int vs = j % kVSt;
+        if (!mbar_wait(v_full + 8 * vs, (j / kVSt) & 1, p.err)) { ok = false; break; }
+        tc::fence_after();
+        const uint32_t vb = sb + kVOff + vs * kTileBytes;
+        const uint32_t pa = tS + (j & 1) * 128;
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k)
+          tc::mma_ts(tO, pa + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o,
+                     (j > 0 || k > 0) ? 1u : 0u);
+        if (splitp)
+#pragma unroll
+          for (int k = 0; k < kBN / 16; ++k)
+            tc::mma_ts(tO, pa + 64 + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o, 1u);
+        tc::commit(o_done);
+        tc::commit(v_empty + 8 * vs);
+      }
+      // every MMA issued has completed before TMEM is released
+      tc::commit(drain);
+      mbar_wait(drain, 0, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax warps ----------------
+    const int row = 32 * (warp & 3) + lane;  // TMEM lane of this thread = query row in the tile
+    const int i = i0 + row;
+    const int pos = past + i;                // position of this row's token
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const T* brow = nullptr;
+    if (p.bias && i < p.S) {
+      const int bb = p.bias_b > 1 ? b : 0, hb = p.bias_h > 1 ? h : 0;
+      brow = static_cast<const T*>(p.bias) + (((size_t)bb * p.bias_h + hb) * p.S + i) * p.total;
+    }
+    const bool bias_vec = brow && (p.total % 8 == 0) && (kstart % 8 == 0) &&
+                          (reinterpret_cast<uintptr_t>(p.bias) & 15) == 0;
+    float m_ref = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int k0 = kstart + j * kBN;
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * (j & 1), (j >> 1) & 1, p.err))) { ok = false; break; }
+      tc::fence_after();
+      const uint32_t tSj = tS + (j & 1) * 128 + lane_off;
+      // scores of this row, scaled into log2 units, with bias and mask
+      float s[kBN];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::ld32(tSj + c * 32, r);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]) * p.scale_log2;
+      }
+      if (brow) {
+        if (bias_vec) {
+#pragma unroll
+          for (int c = 0; c < kBN / 8; ++c) {
+            const int key = k0 + c * 8;
+            if (key < kend) {
+              const VecT<T, 8> bv = *reinterpret_cast<const VecT<T, 8>*>(brow + key);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) s[c * 8 + e] = fmaf(E::to_f(bv.v[e]), kLog2e, s[c * 8 + e]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (k0 + c < kend) s[c] = fmaf(E::to_f(brow[k0 + c]), kLog2e, s[c]);
+        }
+      }
+      // mask: keys after the row's position, before its window, beyond the tile's range
+      const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
+      float mt = -INFINITY;
+      if (edge) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const int key = k0 + c;
+          const bool vis = key <= pos && (p.window <= 0 || key > pos - p.window);
+          s[c] = vis ? s[c] : -INFINITY;
+          mt = fmaxf(mt, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, s[c]);
+      }
+      // running max with lazy rescaling of O
+      const float m_new = fmaxf(m_ref, mt);
+      const bool need = m_new > m_ref + kRescaleThresh;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? fast_exp2(m_ref - m_new) : 1.f;
+        if (need) {
+          m_ref = m_new;
+          l_run *= f;
+        }
+        if (j > 0) {
+          // O holds the sum over earlier tiles once P_{j-1} V_{j-1} has completed
+          // (o_done is then at phase j - 1 or j: S_j completing implies P_{j-2} V_{j-2} has, and
+          // P_j V_j waits for this warp)
+          if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, p.err))) { ok = false; break; }
+          tc::fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tc::ld32(tO + lane_off + c * 32, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
+            tc::st32(tO + lane_off + c * 32, r);
+          }
+          tc::wait_st();
+        }
+      }
+      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      float rs = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < kBN / 2; ++c) {
+        const float a = fast_exp2(s[2 * c] - mu), bq = fast_exp2(s[2 * c + 1] - mu);
+        rs += a + bq;
+        pk[c >> 5][c & 31] = E::pack2(a, bq);
+      }
+      l_run += rs;
+      tc::st32(tSj, pk[0]);
+      tc::st32(tSj + 32, pk[1]);
+      if (splitp) {
+#pragma unroll
+        for (int c = 0; c < kBN / 2; ++c) {
+          const float2 hv = E::unpack2(pk[c >> 5][c & 31]);
+          const float a = fast_exp2(s[2 * c] - mu), bq = fast_exp2(s[2 * c + 1] - mu);
+          pk[c >> 5][c & 31] = E::pack2(a - hv.x, bq - hv.y);
+        }
+        tc::st32(tSj + 64, pk[0]);
+        tc::st32(tSj + 96, pk[1]);
+      }
+      tc::wait_st();
+      // value rows past the sequence's length (the tile can reach beyond it,
+      // whatever the last key the rows see) must not meet P = 0 as NaN
+      if (k0 + kBN > L) {
+        const int vs = j % kVSt;
+        if (!__all_sync(0xffffffffu, mbar_wait(v_full + 8 * vs, (j / kVSt) & 1, p.err))) { ok = false; break; }
+        const int r0 = L - k0;
+        if (row >= r0) {
+          uint8_t* vt = smem + kVOff + vs * kTileBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vt + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vt + kBoxBytes + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      tc::fence_before();
+      mbar_arrive(p_full + 8 * (j & 1));
+    }
+    // epilogue: O / l to the output row, once every MMA has completed (the
+    // single-phase drain barrier; o_done could alias an older phase here)
+    if (ok && __all_sync(0xffffffffu, mbar_wait(drain, 0, p.err))) {
+      tc::fence_after();
+      const float inv = 1.f / l_run;
+      T* orow = static_cast<T*>(p.out) + ((size_t)(b * p.S + i) * p.H + h) * kD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::ld32(tO + lane_off + c * 32, r);
+        tc::wait_ld();
+        if (i < p.S) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = E::pack2(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
+            v.y = E::pack2(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
+            v.z = E::pack2(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
+            v.w = E::pack2(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after();
+    tc::dealloc(tbase, kTmemCols);
+  }
+}
+
+template <typename T>
+cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
+  const CUtensorMapDataType dt =
+      a.dtype == GQA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap qmap, kmap, vmap;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.S, (cuuint64_t)a.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2, (cuuint64_t)a.S * a.H * kD * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
+    if (!encode_tensor_map(&qmap, dt, 4, const_cast<void*>(q_src), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)a.M, (cuuint64_t)a.B * a.Hkv};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)a.M * kD * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)kBN, 1};
+    if (!encode_tensor_map(&kmap, dt, 3, a.kbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&vmap, dt, 3, a.vbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  const int n_qt = (a.S + kBM - 1) / kBM;
+  PrefillParams p{a.err, a.seqlens, a.bias, a.out, a.B, a.S, a.H, a.Hkv, a.M, a.total, a.window, a.bias_b, a.bias_h,
+                  n_qt, a.scale * kLog2e};
+  auto kern = prefill_kernel<T>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const long long nblk = (long long)a.B * a.H * n_qt;
+  kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src) : launch_t<__half>(a, q_src);
+}
+
+}  // namespace gqa

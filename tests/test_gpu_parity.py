@@ -166,6 +166,12 @@ def test_decode_repeat_is_idempotent():
     dict(S=1, D=64, past=(3, 0, 40), M=64, seed=36),
     dict(S=16, D=8, H=4, Hkv=2, past=(0, 4, 8), M=32, interleaved=1, seed=37),
     dict(S=16, D=128, rotary=False, past=(0, 4, 8), M=32, seed=38),
+    # tensor-core prefill: several query and key tiles, ragged tails, bias paths, windows
+    dict(S=200, past=(0, 77, 1000), M=1304, total=1304, dtype="bf16", bias=(1, 1), seed=40),
+    dict(S=200, past=(3, 77, 1001), M=1300, total=1300, dtype="fp16", bias=(3, 8), seed=41),
+    dict(S=129, past=(5, 0, 300), M=512, window=100, bias=(3, 1), seed=42),
+    dict(S=257, past=(0, 130, 255), M=600, window=300, dtype="bf16", seed=43),
+    dict(S=128, past=(128, 0, 383), M=512, H=16, Hkv=2, seed=44),
 ])
 def test_prefill_cases(kw):
     check(custom(**kw))
