@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="workload to time as the headline (default: the batched decode)")
     ap.add_argument("--quick", action="store_true",
                     help="headline workload only: no burn-in, end-to-end leg, other workloads or CPU baseline "
                          "(for profiler runs)")
@@ -231,19 +233,26 @@ def e2e_decode(prob, steps, warmup, stream):
     import torch
     import shared_kv_cache_gb300 as gqa
     d = prob.inp
-    hq, hk, hv = (d[n].cpu().pin_memory() for n in ("query", "key", "value"))
-    hs = d["seqlens_k"].cpu().pin_memory()
+    # the step's host inputs (query, key, value rows and seqlens_k) packed in
+    # one pinned buffer, so that one copy per direction moves them
+    parts = [d[n] for n in ("query", "key", "value")]
+    nbytes = [t.numel() * t.element_size() for t in parts] + [d["seqlens_k"].numel() * 4]
+    offs = [0]
+    for nb in nbytes:
+        offs.append(offs[-1] + (nb + 255) // 256 * 256)
+    host = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
+    for t, o, nb in zip(parts + [d["seqlens_k"]], offs, nbytes):
+        host[o:o + nb].copy_(t.contiguous().view(torch.uint8).reshape(-1).cpu())
+    dev = torch.empty_like(host, device=prob.out.device)
+    views = [dev[o:o + nb].view(t.dtype).view(t.shape) for t, o, nb in zip(parts + [d["seqlens_k"]], offs, nbytes)]
+    dq, dk, dv, ds = views
     hout = torch.empty(prob.out.shape, dtype=prob.out.dtype).pin_memory()
-    dq, dk, dv, ds = (torch.empty_like(d[n]) for n in ("query", "key", "value", "seqlens_k"))
     wsp = gqa.Workspace()
     w = prob.w
 
     def one(i):
         r = i % len(prob.kbufs)
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        ds.copy_(hs, non_blocking=True)
+        dev.copy_(host, non_blocking=True)
         out = gqa.forward(dq, dk, dv, prob.kbufs[r], prob.vbufs[r], ds, prob.total, w.num_heads, w.kv_num_heads,
                           d["cos"], d["sin"], d["scale"], d["local_window_size"], d["attention_bias"],
                           output=prob.out, workspace=wsp, stream=stream)
@@ -261,7 +270,7 @@ def e2e_decode(prob, steps, warmup, stream):
         e1.record(stream)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs))
+    h2d = host.numel()
     d2h = hout.numel() * hout.element_size()
     return ms, h2d, d2h
 
@@ -308,6 +317,24 @@ print(json.dumps({{"value": nbytes * n / dt / 1e9, "calls": n, "seconds": dt, "s
                       f"{res['seconds']:.1f} s (numpy float64, {cores} host threads available)"}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the dominant
+# kernel per launch, from the ncu captures summarised in profiles/; a kernel
+# changed since its capture has no entry (reported as null).
+TRAFFIC = {
+    "decode_b16": 105336832 + 3085312,     # decode_kernel, profiles/decode_kernel_decode_b16.md
+    "prefill_2k": 102152704 + 31195136,    # prefill_kernel, profiles/prefill_kernel_prefill_2k.md
+}
+
+
+def metric_of(prob):
+    """(metric, unit, value per second scale) of a workload: decode steps are
+    HBM-bound and counted in algorithmic KV bytes, prefill steps in attention
+    FLOPs."""
+    if prob.decode:
+        return "GQA decode KV GB/s", "GB/s", prob.bytes / 1e9
+    return "GQA prefill attention TFLOP/s", "TFLOP/s", prob.flops / 1e12
+
+
 def run_ours(args):
     import torch
     rank, ws = dist_init("nccl")
@@ -315,12 +342,18 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     import shared_kv_cache_gb300 as gqa
+    from shared_kv_cache_gb300 import workloads as W
     gqa.load_library()
     pk = peaks()
     stream = torch.cuda.Stream(device)
 
-    # headline: batched decode, rotating four buffer sets (4 x 268 MB > L2)
-    prob = Problem(HEADLINE, device, sets=4)
+    name = args.workload
+    w = W.CONFIGS[name]
+    kv_bytes = 2 * w.batch * w.kv_num_heads * w.max_seq_len * w.head_size * 2
+    # rotate buffer sets so that consecutive steps do not find their KV rows in L2
+    sets = 4 if kv_bytes < (1 << 30) else 1
+    prob = Problem(name, device, sets=sets)
+    metric, unit, work = metric_of(prob)
     sampler = ClockSampler(gpu_selector(torch, local))
     sampler.start()
     # keep the GPU busy for ~1 s before timing so that the clock record reflects load
@@ -335,52 +368,63 @@ def run_ours(args):
     ms, t0, t1 = time_steps(prob, args.steps, max(args.warmup, 3), stream, ws, device)
     sampler.stop()
     clocks = sampler.summary(tb, t1)
-    gbs = prob.bytes / (ms * 1e-3) / 1e9
-    value = gbs * ws
+    rate = work / (ms * 1e-3)
+    value = rate * ws
 
     e2e_ms, h2d, d2h = e2e_decode(prob, args.steps if not args.quick else 1, 1 if args.quick else
                                   max(args.warmup, 3), stream)
-    e2e = {"value": prob.bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+    e2e = {"value": work * ws / (e2e_ms * 1e-3), "unit": unit,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    roofline = {"kernel": "decode_kernel + combine_kernel (one gqa_forward call)", "bound": "hbm",
-                "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
-                "peak_source": pk["source"], "frac_of_nominal_8tbs": gbs / 8000.0,
-                "bytes_per_launch": prob.bytes, "traffic": None}
+    if prob.decode:
+        roofline = {"kernel": "decode_kernel + combine_kernel (one gqa_forward call)", "bound": "hbm",
+                    "achieved": rate, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": rate / pk["hbm_gbs"],
+                    "peak_source": pk["source"], "frac_of_nominal_8tbs": rate / 8000.0,
+                    "bytes_per_launch": prob.bytes, "traffic": TRAFFIC.get(name),
+                    "traffic_kernel": "decode_kernel"}
+    else:
+        roofline = {"kernel": "rope_append_kernel + prefill_kernel (one gqa_forward call)", "bound": "tensor",
+                    "achieved": rate, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": rate / pk["bf16_tflops"], "peak_source": pk["source"],
+                    "flops_per_launch": prob.flops, "traffic": TRAFFIC.get(name),
+                    "traffic_kernel": "prefill_kernel"}
 
     also = []
     if not args.no_also and not args.quick:
-        for name, sets in (("long_decode", 1), ("long_decode_w4096", 4), ("prefill_2k", 1),
-                           ("chunked_prefill", 4)):
-            p = Problem(name, device, sets=sets)
-            steps = 20 if not p.decode else 50
-            m, _, _ = time_steps(p, steps, 3, stream, ws, device)
-            if p.decode:
-                v = p.bytes / (m * 1e-3) / 1e9
-                also.append({"workload": name, "metric": "GQA decode KV GB/s", "value": v, "unit": "GB/s",
-                             "ms_per_step": m, "frac": v / pk["hbm_gbs"], "peak": pk["hbm_gbs"]})
-            else:
-                v = p.flops / (m * 1e-3) / 1e12
-                also.append({"workload": name, "metric": "GQA prefill attention TFLOP/s", "value": v,
-                             "unit": "TFLOP/s", "ms_per_step": m, "frac": v / pk["bf16_tflops"],
-                             "peak": pk["bf16_tflops"], "kv_gbs": p.bytes / (m * 1e-3) / 1e9})
-            del p
+        for other in ("decode_b16", "long_decode", "long_decode_w4096", "prefill_2k", "chunked_prefill"):
+            if other == name:
+                continue
+            wo = W.CONFIGS[other]
+            kvo = 2 * wo.batch * wo.kv_num_heads * wo.max_seq_len * wo.head_size * 2
+            p2 = Problem(other, device, sets=4 if kvo < (1 << 30) else 1)
+            steps = 20 if not p2.decode else 50
+            m, _, _ = time_steps(p2, steps, 3, stream, ws, device)
+            mt, un, wk = metric_of(p2)
+            v = wk / (m * 1e-3)
+            peak = pk["hbm_gbs"] if p2.decode else pk["bf16_tflops"]
+            entry = {"workload": other, "metric": mt, "value": v, "unit": un, "ms_per_step": m,
+                     "frac": v / peak, "peak": peak}
+            if not p2.decode:
+                entry["kv_gbs"] = p2.bytes / (m * 1e-3) / 1e9
+            also.append(entry)
+            del p2
             torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu and not args.quick:
-        cpu = cpu_baseline(HEADLINE)
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.quick and prob.decode:
+        cpu = cpu_baseline(name)
 
-    w = prob.w
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) Q/K/V and cache)",
-        "config": {"workload": HEADLINE, "batch": w.batch, "num_heads": w.num_heads,
+        "config": {"workload": name, "batch": w.batch, "num_heads": w.num_heads,
                    "kv_num_heads": w.kv_num_heads, "head_size": w.head_size, "max_seq_len": w.max_seq_len,
                    "new_tokens": w.seq_len, "past_lengths": f"uniform [{w.past_lo}, {w.past_hi}]",
-                   "rotary": True, "bytes_per_step": prob.bytes,
-                   "l2": "4 rotating KV buffer sets (4 x 268 MB) > 129 MB L2",
+                   "local_window_size": w.local_window_size, "rotary": True,
+                   "bytes_per_step": prob.bytes, "flops_per_step": prob.flops,
+                   "l2": (f"{sets} rotating KV buffer sets ({sets} x {kv_bytes >> 20} MiB)" if sets > 1 else
+                          f"KV buffers of {kv_bytes >> 20} MiB") + " vs 129 MB L2",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": prob.launches_per_step() * args.steps,
