@@ -11,22 +11,26 @@
 // scaled scores (plus bias) weighting the value rows.  The key scan of a query
 // tile stops at the last key its rows can see; it never sweeps max_seq_len.
 //
-// One CTA per (sequence, query head, tile of 128 new tokens).  Warp roles:
-//   warp 0      bulk-tensor (TMA) loads: the query tile once, then the K and V
-//               tiles of 128 keys through two 2-stage rings;
-//   warp 1      owns TMEM; lane 0 issues the MMAs:
-//                 S_j = Q K_j^T            (A, B from shared memory)
-//                 O  += P_j V_j            (A = P_j from TMEM, B = V_j MN-major)
-//               S_{j+1} is issued before P_j V_j, so the tensor core computes
-//               the next scores while the softmax warps work on tile j;
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r), reads its
-//               128 scores, applies scale, bias and mask, updates the running
-//               max and sum, writes P_j (16-bit) over S_j in TMEM, and rescales
-//               O in TMEM only when the row max grew by more than 2^8 (the
-//               un-rescaled terms stay bounded by 2^8 and the final division
-//               uses the same reference max); finally O / l goes to the output.
-// TMEM columns: S_0 [0,128), S_1 [128,256), O [256,384) of a 512-column
-// allocation (one CTA per SM: the shared-memory footprint sees to that).
+// One CTA per (sequence, KV head, pair of query heads of that KV head, tile
+// of 128 new tokens): the two query tiles A and B share every K/V tile the
+// CTA loads.  Warp roles:
+//   warp 0      bulk-tensor (TMA) loads: the two query tiles once, then K and
+//               V tiles of 128 keys through two 2-stage rings;
+//   warp 1      owns TMEM; lane 0 issues the MMAs in the order
+//                 ... P_A(j) V_j, S_A(j+1), P_B(j) V_j, S_B(j+1), ...
+//               (S = Q K^T from shared memory; O += P V with P in TMEM and V
+//               MN-major in shared memory), so the tensor core always has the
+//               other tile's work while one tile's softmax runs (ping-pong);
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: thread r owns
+//               query row r (TMEM lane r).  Pass 1 reads the 128 scores of the
+//               row, applies scale, bias and mask (writing adjusted scores back
+//               when there are any) and takes the row max; pass 2 re-reads
+//               them, exponentiates, sums, and writes P (16-bit) over S.  O is
+//               rescaled in TMEM only when the row max grew by more than 2^8
+//               (the un-rescaled terms stay bounded by 2^8 and the final
+//               division uses the same reference max).
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// With an odd group size the last head of each KV head runs alone (B idle).
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -39,15 +43,16 @@ constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per KV tile
 constexpr int kKSt = 2;    // K ring stages
 constexpr int kVSt = 2;    // V ring stages
-constexpr int kThreads = 192;
-constexpr int kTileBytes = kBN * kD * 2;       // 32 KB: two 128-row x 128-byte boxes
+constexpr int kThreads = 320;
+constexpr int kTileBytes = kBN * kD * 2;  // 32 KB: two 128-row x 128-byte boxes
 constexpr int kBoxBytes = kTileBytes / 2;
-constexpr int kQOff = 0;
-constexpr int kKOff = kQOff + kBM * kD * 2;
+constexpr int kQBytes = kBM * kD * 2;
+constexpr int kQOff = 0;                   // Q_A, then Q_B
+constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKSt * kTileBytes;
 constexpr int kBarOff = kVOff + kVSt * kTileBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done, drain
-constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 1 + 1;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain
+constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1;
 constexpr int kSlotOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kSlotOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -58,7 +63,7 @@ struct PrefillParams {
   const int32_t* seqlens;
   const void* bias;  // [Bb, Hb, S, total] or nullptr
   void* out;         // [B, S, H*D]
-  int B, S, H, Hkv, M, total, window, bias_b, bias_h, n_qt;
+  int B, S, H, Hkv, G, M, total, window, bias_b, bias_h, n_qt, n_pairs;
   float scale_log2;
 };
 
@@ -84,17 +89,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_full = bar0;
   const uint32_t k_full = bar0 + 8, k_empty = k_full + 8 * kKSt;
   const uint32_t v_full = k_empty + 8 * kKSt, v_empty = v_full + 8 * kVSt;
-  const uint32_t s_full = v_empty + 8 * kVSt, p_full = s_full + 16;
-  const uint32_t o_done = p_full + 16, drain = o_done + 8;
+  const uint32_t s_full = v_empty + 8 * kVSt;  // [A, B]
+  const uint32_t p_full = s_full + 16;         // [A, B]
+  const uint32_t o_done = p_full + 16;         // [A, B]
+  const uint32_t drain = o_done + 16;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // work item: heaviest query tiles first
-  const int bh = blockIdx.x % (p.B * p.H);
-  const int qt = p.n_qt - 1 - blockIdx.x / (p.B * p.H);
-  const int b = bh / p.H, h = bh - b * p.H;
-  const int kh = h / (p.H / p.Hkv);
+  const int per_qt = p.B * p.Hkv * p.n_pairs;
+  const int qt = p.n_qt - 1 - (int)(blockIdx.x / per_qt);
+  const int rem = (int)(blockIdx.x % per_qt);
+  const int b = rem / (p.Hkv * p.n_pairs);
+  const int kh = (rem / p.n_pairs) % p.Hkv;
+  const int pr = rem % p.n_pairs;
+  const int hA = kh * p.G + 2 * pr;
+  const bool has_b = 2 * pr + 1 < p.G;
   const int past = p.seqlens[b];
   if (sequence_error(past, p.S, p.M, p.total)) return;  // recorded by the append kernel
   const int i0 = qt * kBM;
@@ -104,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kend = past + i1;  // one past the last key any row of the tile sees
   const int n_kv = (kend - kstart + kBN - 1) / kBN;
   // bf16 tiles whose first row sees few keys also carry P's rounding residue
-  // (P = hi + lo, both bf16; lo in the upper 64 columns of the S buffer) so
+  // (P = hi + lo, both bf16; lo in the upper 64 columns of the S region) so
   // that P.V keeps fp32-level accuracy where a few keys dominate the output
   const int min_keys = p.window > 0 ? min(p.window, past + i0 + 1) : past + i0 + 1;
   const bool splitp = kBF16 && min_keys <= 256;
@@ -122,8 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + 8 * s, 1);
       mbar_init(p_full + 8 * s, 128);
+      mbar_init(o_done + 8 * s, 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     fence_mbar_init();
   }
@@ -132,7 +143,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tbase = *tslot;
-  const uint32_t tS = tbase, tO = tbase + 256;
 
   if (warp == 0) {
     // ---------------- producer ----------------
@@ -140,21 +150,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      mbar_arrive_expect_tx(q_full, kBM * kD * 2);
-      tma_load_4d(sb + kQOff, &qmap, 0, h, i0, b, q_full);
-      tma_load_4d(sb + kQOff + kBoxBytes, &qmap, 64, h, i0, b, q_full);
+      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * kQBytes);
+      tma_load_4d(sb + kQOff, &qmap, 0, hA, i0, b, q_full);
+      tma_load_4d(sb + kQOff + kBoxBytes, &qmap, 64, hA, i0, b, q_full);
+      if (has_b) {
+        tma_load_4d(sb + kQOff + kQBytes, &qmap, 0, hA + 1, i0, b, q_full);
+        tma_load_4d(sb + kQOff + kQBytes + kBoxBytes, &qmap, 64, hA + 1, i0, b, q_full);
+      }
       const int zkv = b * p.Hkv + kh;
       int issued_k = 0, issued_v = 0;
-      bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
+      for (int j = 0; j < n_kv; ++j) {
         const int y = kstart + j * kBN;
         const int ks = j % kKSt, vs = j % kVSt;
-        if (j >= kKSt && !mbar_wait(k_empty + 8 * ks, ((j / kKSt) - 1) & 1, p.err)) { ok = false; break; }
+        if (j >= kKSt && !mbar_wait(k_empty + 8 * ks, ((j / kKSt) - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(k_full + 8 * ks, kTileBytes);
         tma_load_3d(sb + kKOff + ks * kTileBytes, &kmap, 0, y, zkv, k_full + 8 * ks);
         tma_load_3d(sb + kKOff + ks * kTileBytes + kBoxBytes, &kmap, 64, y, zkv, k_full + 8 * ks);
         issued_k = j + 1;
-        if (j >= kVSt && !mbar_wait(v_empty + 8 * vs, ((j / kVSt) - 1) & 1, p.err)) { ok = false; break; }
+        if (j >= kVSt && !mbar_wait(v_empty + 8 * vs, ((j / kVSt) - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(v_full + 8 * vs, kTileBytes);
         tma_load_3d(sb + kVOff + vs * kTileBytes, &vmap, 0, y, zkv, v_full + 8 * vs);
         tma_load_3d(sb + kVOff + vs * kTileBytes + kBoxBytes, &vmap, 64, y, zkv, v_full + 8 * vs);
@@ -162,8 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no copy may still be in flight into shared memory when the CTA exits
       mbar_wait(q_full, 0, p.err);
-      for (int j = max(0, issued_k - kKSt); j < issued_k; ++j) mbar_wait(k_full + 8 * (j % kKSt), (j / kKSt) & 1, p.err);
-      for (int j = max(0, issued_v - kVSt); j < issued_v; ++j) mbar_wait(v_full + 8 * (j % kVSt), (j / kVSt) & 1, p.err);
+      for (int j = max(0, issued_k - kKSt); j < issued_k; ++j)
+        mbar_wait(k_full + 8 * (j % kKSt), (j / kKSt) & 1, p.err);
+      for (int j = max(0, issued_v - kVSt); j < issued_v; ++j)
+        mbar_wait(v_full + 8 * (j % kVSt), (j / kVSt) & 1, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -171,42 +186,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = tc::idesc_f16(kBF16, kBM, kBN, false, false);
       const uint32_t id_o = tc::idesc_f16(kBF16, kBM, kD, false, true);
-      bool ok = mbar_wait(q_full, 0, p.err);
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % kKSt;
-        if (!mbar_wait(k_full + 8 * ks, (j / kKSt) & 1, p.err)) return false;
-        tc::fence_after();
-        const uint32_t qa = sb + kQOff, kb = sb + kKOff + ks * kTileBytes;
-        const uint32_t d = tS + (j & 1) * 128;
+      const int ntile = has_b ? 2 : 1;
+      auto issue_s = [&](int j, int t) {  // S_t = Q_t K_j^T into TMEM S region t
+        const uint32_t qa = sb + kQOff + t * kQBytes, kb = sb + kKOff + (j % kKSt) * kTileBytes;
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
           const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
-          tc::mma_ss(d, tc::smem_desc(qa + off, 16, 1024, tc::kSwizzle128B),
+          tc::mma_ss(tbase + t * 128, tc::smem_desc(qa + off, 16, 1024, tc::kSwizzle128B),
                      tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), id_s, k > 0 ? 1u : 0u);
         }
-        tc::commit(s_full + 8 * (j & 1));
-        tc::commit(k_empty + 8 * ks);
-        return true;
+        tc::commit(s_full + 8 * t);
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !issue_s(j + 1)) { ok = false; break; }
-        if (!mbar_wait(p_full + 8 * (j & 1), (j >> 1) & 1, p.err)) { ok = false; break; }
-        const int vs = j % kVSt;
-        if (!mbar_wait(v_full + 8 * vs, (j / kVSt) & 1, p.err)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t vb = sb + kVOff + vs * kTileBytes;
-        const uint32_t pa = tS + (j & 1) * 128;
+      auto issue_pv = [&](int j, int t) {  // O_t += P_t V_j
+        const uint32_t vb = sb + kVOff + (j % kVSt) * kTileBytes;
+        const uint32_t pa = tbase + t * 128;
+        const uint32_t od = tbase + 256 + t * 128;
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          tc::mma_ts(tO, pa + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o,
+          tc::mma_ts(od, pa + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o,
                      (j > 0 || k > 0) ? 1u : 0u);
         if (splitp)
 #pragma unroll
           for (int k = 0; k < kBN / 16; ++k)
-            tc::mma_ts(tO, pa + 64 + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o, 1u);
-        tc::commit(o_done);
-        tc::commit(v_empty + 8 * vs);
+            tc::mma_ts(od, pa + 64 + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o,
+                       1u);
+        tc::commit(o_done + 8 * t);
+      };
+      bool ok = mbar_wait(q_full, 0, p.err) && mbar_wait(k_full, 0, p.err);
+      if (ok) {
+        tc::fence_after();
+        for (int t = 0; t < ntile; ++t) issue_s(0, t);
+        tc::commit(k_empty);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const bool more = j + 1 < n_kv;
+        if (!mbar_wait(v_full + 8 * (j % kVSt), (j / kVSt) & 1, p.err)) break;
+        for (int t = 0; t < ntile && ok; ++t) {
+          if (!mbar_wait(p_full + 8 * t, j & 1, p.err)) { ok = false; break; }
+          tc::fence_after();
+          issue_pv(j, t);
+          if (more) {
+            // S_t(j+1) overwrites S_t / P_t(j) after P_t(j) V_j in issue order
+            if (t == 0 && !mbar_wait(k_full + 8 * ((j + 1) % kKSt), ((j + 1) / kKSt) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after();
+            issue_s(j + 1, t);
+          }
+        }
+        if (!ok) break;
+        tc::commit(v_empty + 8 * (j % kVSt));
+        if (more) tc::commit(k_empty + 8 * ((j + 1) % kKSt));
       }
       // every MMA issued has completed before TMEM is released
       tc::commit(drain);
@@ -214,11 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- softmax warps ----------------
+    // ---------------- softmax warps: 2..5 tile A, 6..9 tile B ----------------
+    const int t = (warp - 2) >> 2;           // tile of this warpgroup
     const int row = 32 * (warp & 3) + lane;  // TMEM lane of this thread = query row in the tile
     const int i = i0 + row;
-    const int pos = past + i;                // position of this row's token
+    const int h = hA + t;
+    const int pos = past + i;  // position of this row's token
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t tS = tbase + t * 128 + lane_off;
+    const uint32_t tO = tbase + 256 + t * 128 + lane_off;
     const T* brow = nullptr;
     if (p.bias && i < p.S) {
       const int bb = p.bias_b > 1 ? b : 0, hb = p.bias_h > 1 ? h : 0;
@@ -227,54 +262,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool bias_vec = brow && (p.total % 8 == 0) && (kstart % 8 == 0) &&
                           (reinterpret_cast<uintptr_t>(p.bias) & 15) == 0;
     float m_ref = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    const bool active = t == 0 || has_b;
+    bool ok = active;
+    for (int j = 0; j < n_kv && ok; ++j) {
       const int k0 = kstart + j * kBN;
-      if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * (j & 1), (j >> 1) & 1, p.err))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * t, j & 1, p.err))) { ok = false; break; }
       tc::fence_after();
-      const uint32_t tSj = tS + (j & 1) * 128 + lane_off;
-      // scores of this row, scaled into log2 units, with bias and mask
-      float s[kBN];
+      // pass 1: scale, bias, mask (written back when they change the scores), row max
+      const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
+      // (uniform across the warp: the TMEM stores below are warp-collective;
+      // rows past S have no bias row and add zero)
+      const bool adjust = edge || p.bias != nullptr;
+      float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tc::ld32(tSj + c * 32, r);
+        tc::ld32(tS + c * 32, r);
         tc::wait_ld();
+        if (adjust) {
+          float bv[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]) * p.scale_log2;
-      }
-      if (brow) {
-        if (bias_vec) {
+          for (int e = 0; e < 32; ++e) bv[e] = 0.f;
+          if (brow) {
+            if (bias_vec) {
 #pragma unroll
-          for (int c = 0; c < kBN / 8; ++c) {
-            const int key = k0 + c * 8;
-            if (key < kend) {
-              const VecT<T, 8> bv = *reinterpret_cast<const VecT<T, 8>*>(brow + key);
+              for (int q = 0; q < 4; ++q) {
+                const int key = k0 + c * 32 + q * 8;
+                if (key < kend) {
+                  const VecT<T, 8> v8 = *reinterpret_cast<const VecT<T, 8>*>(brow + key);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) s[c * 8 + e] = fmaf(E::to_f(bv.v[e]), kLog2e, s[c * 8 + e]);
+                  for (int e = 0; e < 8; ++e) bv[q * 8 + e] = E::to_f(v8.v[e]);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                if (k0 + c * 32 + e < kend) bv[e] = E::to_f(brow[k0 + c * 32 + e]);
             }
           }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int key = k0 + c * 32 + e;
+            float v = fmaf(bv[e], kLog2e, __uint_as_float(r[e]) * p.scale_log2);
+            const bool vis = key <= pos && (p.window <= 0 || key > pos - p.window);
+            v = vis ? v : -INFINITY;
+            mt = fmaxf(mt, v);
+            r[e] = __float_as_uint(v);
+          }
+          tc::st32(tS + c * 32, r);
         } else {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (k0 + c < kend) s[c] = fmaf(E::to_f(brow[k0 + c]), kLog2e, s[c]);
+          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(r[e]));
         }
       }
-      // mask: keys after the row's position, before its window, beyond the tile's range
-      const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
-      float mt = -INFINITY;
-      if (edge) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int key = k0 + c;
-          const bool vis = key <= pos && (p.window <= 0 || key > pos - p.window);
-          s[c] = vis ? s[c] : -INFINITY;
-          mt = fmaxf(mt, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) mt = fmaxf(mt, s[c]);
-      }
+      if (adjust)
+        tc::wait_st();
+      else
+        mt *= p.scale_log2;
       // running max with lazy rescaling of O
       const float m_new = fmaxf(m_ref, mt);
       const bool need = m_new > m_ref + kRescaleThresh;
@@ -285,46 +329,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           l_run *= f;
         }
         if (j > 0) {
-          // O holds the sum over earlier tiles once P_{j-1} V_{j-1} has completed
-          // (o_done is then at phase j - 1 or j: S_j completing implies P_{j-2} V_{j-2} has, and
-          // P_j V_j waits for this warp)
-          if (!__all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, p.err))) { ok = false; break; }
+          // O_t holds the earlier tiles' sum once P_t(j-1) V_(j-1) has completed
+          // (o_done_t is then at phase j - 1 or j: S_t(j) was issued after it)
+          if (!__all_sync(0xffffffffu, mbar_wait(o_done + 8 * t, (j - 1) & 1, p.err))) { ok = false; break; }
           tc::fence_after();
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t r[32];
-            tc::ld32(tO + lane_off + c * 32, r);
+            tc::ld32(tO + c * 32, r);
             tc::wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-            tc::st32(tO + lane_off + c * 32, r);
+            tc::st32(tO + c * 32, r);
           }
           tc::wait_st();
         }
       }
+      // pass 2: P = 2^(s - m) (16-bit) over S; chunk c's P columns [16c, 16c+16)
+      // only overwrite scores that have been read already
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      const float sc = adjust ? 1.f : p.scale_log2;
       float rs = 0.f;
-      uint32_t pk[2][32];
+      uint32_t lo[4][16];
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
-        const float a = fast_exp2(s[2 * c] - mu), bq = fast_exp2(s[2 * c + 1] - mu);
-        rs += a + bq;
-        pk[c >> 5][c & 31] = E::pack2(a, bq);
-      }
-      l_run += rs;
-      tc::st32(tSj, pk[0]);
-      tc::st32(tSj + 32, pk[1]);
-      if (splitp) {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::ld32(tS + c * 32, r);
+        tc::wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < kBN / 2; ++c) {
-          const float2 hv = E::unpack2(pk[c >> 5][c & 31]);
-          const float a = fast_exp2(s[2 * c] - mu), bq = fast_exp2(s[2 * c + 1] - mu);
-          pk[c >> 5][c & 31] = E::pack2(a - hv.x, bq - hv.y);
+        for (int e = 0; e < 16; ++e) {
+          const float a = fast_exp2(__uint_as_float(r[2 * e]) * sc - mu);
+          const float bq = fast_exp2(__uint_as_float(r[2 * e + 1]) * sc - mu);
+          rs += a + bq;
+          pk[e] = E::pack2(a, bq);
+          if (splitp) {
+            const float2 hv = E::unpack2(pk[e]);
+            lo[c][e] = E::pack2(a - hv.x, bq - hv.y);
+          }
         }
-        tc::st32(tSj + 64, pk[0]);
-        tc::st32(tSj + 96, pk[1]);
+        tc::st16(tS + c * 16, pk);
       }
+      if (splitp)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::st16(tS + 64 + c * 16, lo[c]);
       tc::wait_st();
+      l_run += rs;
       // value rows past the sequence's length (the tile can reach beyond it,
       // whatever the last key the rows see) must not meet P = 0 as NaN
       if (k0 + kBN > L) {
@@ -342,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       tc::fence_before();
-      mbar_arrive(p_full + 8 * (j & 1));
+      mbar_arrive(p_full + 8 * t);
     }
     // epilogue: O / l to the output row, once every MMA has completed (the
     // single-phase drain barrier; o_done could alias an older phase here)
@@ -353,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tc::ld32(tO + lane_off + c * 32, r);
+        tc::ld32(tO + c * 32, r);
         tc::wait_ld();
         if (i < p.S) {
 #pragma unroll
@@ -398,8 +448,10 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
       return cudaErrorInvalidValue;
   }
   const int n_qt = (a.S + kBM - 1) / kBM;
-  PrefillParams p{a.err, a.seqlens, a.bias, a.out, a.B, a.S, a.H, a.Hkv, a.M, a.total, a.window, a.bias_b, a.bias_h,
-                  n_qt, a.scale * kLog2e};
+  const int G = a.H / a.Hkv;
+  const int n_pairs = (G + 1) / 2;
+  PrefillParams p{a.err, a.seqlens, a.bias, a.out, a.B, a.S, a.H, a.Hkv, G, a.M, a.total, a.window, a.bias_b,
+                  a.bias_h, n_qt, n_pairs, a.scale * kLog2e};
   auto kern = prefill_kernel<T>;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -409,7 +461,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  const long long nblk = (long long)a.B * a.H * n_qt;
+  const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt;
   kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, p);
   return cudaGetLastError();
 }
