@@ -21,7 +21,8 @@
 //               (S = Q K^T from shared memory; O += P V with P in TMEM and V
 //               MN-major in shared memory), so the tensor core always has the
 //               other tile's work while one tile's softmax runs (ping-pong);
-//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B: thread r owns
+//   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B (warps 2, 3
+//               idle; the register split favours the softmax warpgroups): thread r owns
 //               query row r (TMEM lane r).  Pass 1 reads the 128 scores of the
 //               row, applies scale, bias and mask (writing adjusted scores back
 //               when there are any) and takes the row max; pass 2 re-reads
@@ -31,6 +32,8 @@
 //               division uses the same reference max).
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // With an odd group size the last head of each KV head runs alone (B idle).
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -43,7 +46,12 @@ constexpr int kBM = 128;   // query rows per tile
 constexpr int kBN = 128;   // keys per KV tile
 constexpr int kKSt = 2;    // K ring stages
 constexpr int kVSt = 2;    // V ring stages
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // three warpgroups
+// Register split (setmaxnreg): the producer/MMA warpgroup gives registers up
+// to the two softmax warpgroups.  128 * 40 + 256 * 232 = 64512 registers, the
+// launch's 384 threads x 168.
+constexpr int kRegsLow = 40;
+constexpr int kRegsHigh = 232;
 constexpr int kTileBytes = kBN * kD * 2;  // 32 KB: two 128-row x 128-byte boxes
 constexpr int kBoxBytes = kTileBytes / 2;
 constexpr int kQBytes = kBM * kD * 2;
@@ -56,6 +64,10 @@ constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1;
 constexpr int kSlotOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kSlotOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
+#ifndef GQA_PREFILL_POLY_EVERY
+#define GQA_PREFILL_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = GQA_PREFILL_POLY_EVERY;  // 0: every exponential on the special-function unit
 constexpr float kRescaleThresh = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 struct PrefillParams {
@@ -144,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after();
   const uint32_t tbase = *tslot;
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0) {
@@ -187,29 +201,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t id_s = tc::idesc_f16(kBF16, kBM, kBN, false, false);
       const uint32_t id_o = tc::idesc_f16(kBF16, kBM, kD, false, true);
       const int ntile = has_b ? 2 : 1;
+      // descriptor words, computed once: per MMA the issue loop only adds a
+      // constant to a low word (the issuing thread shares its scheduler with
+      // two softmax warps and must keep up with one MMA per 64 cycles)
+      constexpr uint32_t kHi = tc::desc_hi(1024, tc::kSwizzle128B);
+      const uint32_t q_lo0 = tc::desc_lo(sb + kQOff, 16);
+      const uint32_t k_lo0 = tc::desc_lo(sb + kKOff, 16);
+      const uint32_t v_lo0 = tc::desc_lo(sb + kVOff, kBoxBytes);
       auto issue_s = [&](int j, int t) {  // S_t = Q_t K_j^T into TMEM S region t
-        const uint32_t qa = sb + kQOff + t * kQBytes, kb = sb + kKOff + (j % kKSt) * kTileBytes;
+        const uint32_t qa = q_lo0 + t * (kQBytes >> 4), kb = k_lo0 + (j % kKSt) * (kTileBytes >> 4);
+        const uint32_t d = tbase + t * 128;
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
-          const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
-          tc::mma_ss(tbase + t * 128, tc::smem_desc(qa + off, 16, 1024, tc::kSwizzle128B),
-                     tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), id_s, k > 0 ? 1u : 0u);
+          const uint32_t off = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;
+          tc::mma_ss(d, qa + off, kb + off, kHi, id_s, k > 0 ? 1u : 0u);
         }
         tc::commit(s_full + 8 * t);
       };
       auto issue_pv = [&](int j, int t) {  // O_t += P_t V_j
-        const uint32_t vb = sb + kVOff + (j % kVSt) * kTileBytes;
+        const uint32_t vb = v_lo0 + (j % kVSt) * (kTileBytes >> 4);
         const uint32_t pa = tbase + t * 128;
         const uint32_t od = tbase + 256 + t * 128;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k)
-          tc::mma_ts(od, pa + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o,
-                     (j > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kBN / 16; ++k) tc::mma_ts(od, pa + k * 8, vb + k * (2048 >> 4), kHi, id_o, k > 0 ? 1u : acc0);
         if (splitp)
 #pragma unroll
-          for (int k = 0; k < kBN / 16; ++k)
-            tc::mma_ts(od, pa + 64 + k * 8, tc::smem_desc(vb + k * 2048, kBoxBytes, 1024, tc::kSwizzle128B), id_o,
-                       1u);
+          for (int k = 0; k < kBN / 16; ++k) tc::mma_ts(od, pa + 64 + k * 8, vb + k * (2048 >> 4), kHi, id_o, 1u);
         tc::commit(o_done + 8 * t);
       };
       bool ok = mbar_wait(q_full, 0, p.err) && mbar_wait(k_full, 0, p.err);
@@ -244,9 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, p.err);
     }
     __syncwarp();
+  }  // warps 2 and 3 have no role
   } else {
-    // ---------------- softmax warps: 2..5 tile A, 6..9 tile B ----------------
-    const int t = (warp - 2) >> 2;           // tile of this warpgroup
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    // ---------------- softmax warps: 4..7 tile A, 8..11 tile B ----------------
+    const int t = (warp - 4) >> 2;           // tile of this warpgroup
     const int row = 32 * (warp & 3) + lane;  // TMEM lane of this thread = query row in the tile
     const int i = i0 + row;
     const int h = hA + t;
@@ -268,113 +288,151 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = kstart + j * kBN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * t, j & 1, p.err))) { ok = false; break; }
       tc::fence_after();
-      // pass 1: scale, bias, mask (written back when they change the scores), row max
       const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
-      // (uniform across the warp: the TMEM stores below are warp-collective;
-      // rows past S have no bias row and add zero)
-      const bool adjust = edge || p.bias != nullptr;
-      float mt = -INFINITY;
+      const bool adjust = edge || p.bias != nullptr;  // scale, bias and mask applied per score
+      if (adjust) {
+        // Tiles with a mask edge or a bias: rewrite the scores in TMEM,
+        // scaled to log2 units, biased and masked, 32 columns at a time (a
+        // separate pass keeps this code out of the common path below).
+        // Column e of the tile is visible when e <= vis_hi and e > vis_lo.
+        const int vis_hi = pos - k0;
+        const int vis_lo = p.window > 0 ? pos - p.window - k0 : -1;
+        // 32 bias values per chunk, two 16-bit values per word (rows past S
+        // have no bias row and add zero); the next chunk's are requested
+        // before this chunk is processed
+        auto load_bias = [&](int c, uint4 (&d)[4]) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tc::ld32(tS + c * 32, r);
-        tc::wait_ld();
-        if (adjust) {
-          float bv[32];
+          for (int q = 0; q < 4; ++q) {
+            const int key = k0 + c * 32 + q * 8;
+            d[q] = key < kend ? *reinterpret_cast<const uint4*>(brow + key) : make_uint4(0, 0, 0, 0);
+          }
+        };
+        uint4 bcur[4], bnext[4];
+        if (bias_vec) load_bias(0, bcur);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) bv[e] = 0.f;
-          if (brow) {
-            if (bias_vec) {
+        for (int c = 0; c < 4; ++c) {
+          if (bias_vec && c < 3) load_bias(c + 1, bnext);
+          uint32_t r[32];
+          tc::ld32(tS + c * 32, r);
+          uint32_t bw[16];
+          if (bias_vec) {
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int key = k0 + c * 32 + q * 8;
-                if (key < kend) {
-                  const VecT<T, 8> v8 = *reinterpret_cast<const VecT<T, 8>*>(brow + key);
+            for (int q = 0; q < 4; ++q) {
+              bw[4 * q] = bcur[q].x;
+              bw[4 * q + 1] = bcur[q].y;
+              bw[4 * q + 2] = bcur[q].z;
+              bw[4 * q + 3] = bcur[q].w;
+            }
+          } else {
 #pragma unroll
-                  for (int e = 0; e < 8; ++e) bv[q * 8 + e] = E::to_f(v8.v[e]);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                if (k0 + c * 32 + e < kend) bv[e] = E::to_f(brow[k0 + c * 32 + e]);
+            for (int e = 0; e < 16; ++e) {
+              const int key = k0 + c * 32 + 2 * e;
+              const float b0 = (brow && key < kend) ? E::to_f(brow[key]) : 0.f;
+              const float b1 = (brow && key + 1 < kend) ? E::to_f(brow[key + 1]) : 0.f;
+              bw[e] = E::pack2(b0, b1);
             }
           }
+          tc::wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int key = k0 + c * 32 + e;
-            float v = fmaf(bv[e], kLog2e, __uint_as_float(r[e]) * p.scale_log2);
-            const bool vis = key <= pos && (p.window <= 0 || key > pos - p.window);
-            v = vis ? v : -INFINITY;
-            mt = fmaxf(mt, v);
-            r[e] = __float_as_uint(v);
+            const float2 b2 = E::unpack2(bw[e >> 1]);
+            const float bval = (e & 1) ? b2.y : b2.x;
+            const float v = fmaf(bval, kLog2e, __uint_as_float(r[e]) * p.scale_log2);
+            const bool vis = c * 32 + e <= vis_hi && c * 32 + e > vis_lo;
+            r[e] = __float_as_uint(vis ? v : -INFINITY);
           }
           tc::st32(tS + c * 32, r);
-        } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(r[e]));
+          for (int q = 0; q < 4; ++q) bcur[q] = bnext[q];
         }
-      }
-      if (adjust)
         tc::wait_st();
-      else
-        mt *= p.scale_log2;
-      // running max with lazy rescaling of O
+      }
+      // the row's 128 scores, all in registers (one wait for four loads)
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sv[c]);
+      tc::wait_ld();
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sv[c][e]));
+      float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      if (!adjust) mt *= p.scale_log2;  // scale > 0: the max of the scaled scores
+      // running max with lazy rescaling of O (the rescale itself is done
+      // below, once P has left the registers)
       const float m_new = fmaxf(m_ref, mt);
       const bool need = m_new > m_ref + kRescaleThresh;
-      if (__any_sync(0xffffffffu, need)) {
-        const float f = need ? fast_exp2(m_ref - m_new) : 1.f;
-        if (need) {
-          m_ref = m_new;
-          l_run *= f;
-        }
-        if (j > 0) {
-          // O_t holds the earlier tiles' sum once P_t(j-1) V_(j-1) has completed
-          // (o_done_t is then at phase j - 1 or j: S_t(j) was issued after it)
-          if (!__all_sync(0xffffffffu, mbar_wait(o_done + 8 * t, (j - 1) & 1, p.err))) { ok = false; break; }
-          tc::fence_after();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tc::ld32(tO + c * 32, r);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f);
-            tc::st32(tO + c * 32, r);
-          }
-          tc::wait_st();
-        }
+      const bool any_need = __any_sync(0xffffffffu, need);
+      const float f_resc = need ? fast_exp2(m_ref - m_new) : 1.f;
+      if (need) {
+        m_ref = m_new;
+        l_run *= f_resc;
       }
-      // pass 2: P = 2^(s - m) (16-bit) over S; chunk c's P columns [16c, 16c+16)
-      // only overwrite scores that have been read already
+      // P = 2^(s - m) as 16-bit pairs over the first 64 columns of S (every
+      // score is already in registers); one pair in kPolyEvery is
+      // exponentiated on the FMA pipe to relieve the special-function unit
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       const float sc = adjust ? 1.f : p.scale_log2;
-      float rs = 0.f;
-      uint32_t lo[4][16];
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // (two instantiations, so that the common case carries no residue code)
+      auto make_p = [&](auto split_c) {
+        constexpr bool kSplit = decltype(split_c)::value;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tc::ld32(tS + c * 32, r);
-        tc::wait_ld();
-        uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a = fast_exp2(__uint_as_float(r[2 * e]) * sc - mu);
-          const float bq = fast_exp2(__uint_as_float(r[2 * e + 1]) * sc - mu);
-          rs += a + bq;
-          pk[e] = E::pack2(a, bq);
-          if (splitp) {
-            const float2 hv = E::unpack2(pk[e]);
-            lo[c][e] = E::pack2(a - hv.x, bq - hv.y);
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = fmaf(__uint_as_float(sv[c][2 * e]), sc, -mu);
+            const float x1 = fmaf(__uint_as_float(sv[c][2 * e + 1]), sc, -mu);
+            const bool poly = kPolyEvery > 0 && (e % kPolyEvery) == kPolyEvery - 1;
+            const float a = poly ? exp2_poly(x0) : fast_exp2(x0);
+            const float bb = poly ? exp2_poly(x1) : fast_exp2(x1);
+            rs[e & 3] += a + bb;
+            pk[e] = E::pack2(a, bb);
+            if (kSplit) {  // keep P in fp32 for its rounding residue below
+              sv[c][2 * e] = __float_as_uint(a);
+              sv[c][2 * e + 1] = __float_as_uint(bb);
+            }
+          }
+          tc::st16(tS + c * 16, pk);
+        }
+        if (kSplit) {
+          // P's rounding residue (P = hi + lo, both 16-bit) in columns [64, 128)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float a = __uint_as_float(sv[c][2 * e]), bb = __uint_as_float(sv[c][2 * e + 1]);
+              const float2 hv = E::unpack2(E::pack2(a, bb));
+              lo[e] = E::pack2(a - hv.x, bb - hv.y);
+            }
+            tc::st16(tS + 64 + c * 16, lo);
           }
         }
-        tc::st16(tS + c * 16, pk);
-      }
+      };
       if (splitp)
+        make_p(std::true_type{});
+      else
+        make_p(std::false_type{});
+      l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      if (any_need && j > 0) {
+        // O_t holds the earlier tiles' sum once P_t(j-1) V_(j-1) has completed
+        // (o_done_t is then at phase j - 1 or j: S_t(j) was issued after it)
+        if (!__all_sync(0xffffffffu, mbar_wait(o_done + 8 * t, (j - 1) & 1, p.err))) { ok = false; break; }
+        tc::fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::st16(tS + 64 + c * 16, lo[c]);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tc::ld32(tO + c * 32, r);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * f_resc);
+          tc::st32(tO + c * 32, r);
+        }
+      }
       tc::wait_st();
-      l_run += rs;
       // value rows past the sequence's length (the tile can reach beyond it,
       // whatever the last key the rows see) must not meet P = 0 as NaN
       if (k0 + kBN > L) {
