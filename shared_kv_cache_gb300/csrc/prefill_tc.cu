@@ -88,7 +88,9 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-template <typename T>
+// kBias: the call has an attention_bias (a separate instantiation, so that
+// calls without one carry no bias code)
+template <typename T, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -275,31 +277,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tbase + t * 128 + lane_off;
     const uint32_t tO = tbase + 256 + t * 128 + lane_off;
     const T* brow = nullptr;
-    if (p.bias && i < p.S) {
+    if (kBias && i < p.S) {
       const int bb = p.bias_b > 1 ? b : 0, hb = p.bias_h > 1 ? h : 0;
       brow = static_cast<const T*>(p.bias) + (((size_t)bb * p.bias_h + hb) * p.S + i) * p.total;
     }
-    const bool bias_vec = brow && (p.total % 8 == 0) && (kstart % 8 == 0) &&
+    const bool bias_vec = kBias && brow && (p.total % 8 == 0) && (kstart % 8 == 0) &&
                           (reinterpret_cast<uintptr_t>(p.bias) & 15) == 0;
     float m_ref = -INFINITY, l_run = 0.f;
     const bool active = t == 0 || has_b;
     bool ok = active;
+    const float bias_unit = kLog2e / p.scale_log2;  // bias in raw score units (scale > 0)
     for (int j = 0; j < n_kv && ok; ++j) {
       const int k0 = kstart + j * kBN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * t, j & 1, p.err))) { ok = false; break; }
       tc::fence_after();
       const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
-      const bool adjust = edge || p.bias != nullptr;  // scale, bias and mask applied per score
+      const bool adjust = edge || kBias;  // bias and mask applied per score
       if (adjust) {
-        // Tiles with a mask edge or a bias: rewrite the scores in TMEM,
-        // scaled to log2 units, biased and masked, 32 columns at a time (a
-        // separate pass keeps this code out of the common path below).
-        // Column e of the tile is visible when e <= vis_hi and e > vis_lo.
+        // Tiles with a mask edge or a bias: rewrite the scores in TMEM, still
+        // in raw units (s + b log2(e) / scale, or -inf where masked), 32
+        // columns at a time; a separate pass keeps this code out of the
+        // common path below.  Column e of the tile is visible when
+        // e <= vis_hi and e > vis_lo.  Without a bias, a chunk that the whole
+        // warp sees is left as it is and one that it cannot see is only
+        // overwritten.
         const int vis_hi = pos - k0;
         const int vis_lo = p.window > 0 ? pos - p.window - k0 : -1;
-        // 32 bias values per chunk, two 16-bit values per word (rows past S
-        // have no bias row and add zero); the next chunk's are requested
-        // before this chunk is processed
+        constexpr bool has_bias = kBias;
+        // 32 bias values per chunk (16-byte loads), the next chunk's
+        // requested before this chunk is processed
         auto load_bias = [&](int c, uint4 (&d)[4]) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -312,34 +318,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (bias_vec && c < 3) load_bias(c + 1, bnext);
+          const bool all_vis = __all_sync(0xffffffffu, c * 32 + 31 <= vis_hi && c * 32 > vis_lo);
+          const bool none_vis = __all_sync(0xffffffffu, c * 32 > vis_hi || c * 32 + 31 <= vis_lo);
+          if (!has_bias && all_vis) continue;
           uint32_t r[32];
-          tc::ld32(tS + c * 32, r);
-          uint32_t bw[16];
-          if (bias_vec) {
+          if (none_vis) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              bw[4 * q] = bcur[q].x;
-              bw[4 * q + 1] = bcur[q].y;
-              bw[4 * q + 2] = bcur[q].z;
-              bw[4 * q + 3] = bcur[q].w;
-            }
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(-INFINITY);
           } else {
+            tc::ld32(tS + c * 32, r);
+            uint32_t bw[16];
+            if (bias_vec) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int key = k0 + c * 32 + 2 * e;
-              const float b0 = (brow && key < kend) ? E::to_f(brow[key]) : 0.f;
-              const float b1 = (brow && key + 1 < kend) ? E::to_f(brow[key + 1]) : 0.f;
-              bw[e] = E::pack2(b0, b1);
+              for (int q = 0; q < 4; ++q) {
+                bw[4 * q] = bcur[q].x;
+                bw[4 * q + 1] = bcur[q].y;
+                bw[4 * q + 2] = bcur[q].z;
+                bw[4 * q + 3] = bcur[q].w;
+              }
+            } else if (kBias) {
+              // rows past S (no bias row: they add zero), or a bias whose
+              // rows are not 16-byte aligned
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                const int key = k0 + c * 32 + 2 * e;
+                const float b0 = (brow && key < kend) ? E::to_f(brow[key]) : 0.f;
+                const float b1 = (brow && key + 1 < kend) ? E::to_f(brow[key + 1]) : 0.f;
+                bw[e] = E::pack2(b0, b1);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) bw[e] = 0u;
             }
-          }
-          tc::wait_ld();
+            tc::wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float2 b2 = E::unpack2(bw[e >> 1]);
-            const float bval = (e & 1) ? b2.y : b2.x;
-            const float v = fmaf(bval, kLog2e, __uint_as_float(r[e]) * p.scale_log2);
-            const bool vis = c * 32 + e <= vis_hi && c * 32 + e > vis_lo;
-            r[e] = __float_as_uint(vis ? v : -INFINITY);
+            for (int e = 0; e < 32; ++e) {
+              const float2 b2 = E::unpack2(bw[e >> 1]);
+              const float bval = (e & 1) ? b2.y : b2.x;
+              const float v = fmaf(bval, bias_unit, __uint_as_float(r[e]));
+              const bool vis = c * 32 + e <= vis_hi && c * 32 + e > vis_lo;
+              r[e] = __float_as_uint(vis ? v : -INFINITY);
+            }
           }
           tc::st32(tS + c * 32, r);
 #pragma unroll
@@ -357,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sv[c][e]));
-      float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      if (!adjust) mt *= p.scale_log2;  // scale > 0: the max of the scaled scores
+      // (scale > 0: the max of the scaled scores)
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       // running max with lazy rescaling of O (the rescale itself is done
       // below, once P has left the registers)
       const float m_new = fmaxf(m_ref, mt);
@@ -373,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // score is already in registers); one pair in kPolyEvery is
       // exponentiated on the FMA pipe to relieve the special-function unit
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      const float sc = adjust ? 1.f : p.scale_log2;
+      const float sc = p.scale_log2;
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
       // (two instantiations, so that the common case carries no residue code)
       auto make_p = [&](auto split_c) {
@@ -510,14 +529,15 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
   const int n_pairs = (G + 1) / 2;
   PrefillParams p{a.err, a.seqlens, a.bias, a.out, a.B, a.S, a.H, a.Hkv, G, a.M, a.total, a.window, a.bias_b,
                   a.bias_h, n_qt, n_pairs, a.scale * kLog2e};
-  auto kern = prefill_kernel<T>;
-  static bool attr_set[64] = {};
+  auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
+  static bool attr_set[64][2] = {};  // per device and instantiation
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+  const int vi = a.bias ? 1 : 0;
+  if (dev < 0 || dev >= 64 || !attr_set[dev][vi]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev][vi] = true;
   }
   const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt;
   kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, p);
