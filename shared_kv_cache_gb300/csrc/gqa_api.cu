@@ -113,7 +113,9 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
     return pl;
   }
   pl.path = (S > 1 && D == 128) ? Path::kPrefillTC : Path::kGeneric;
-  if (rotary) {
+  // the tensor-core prefill rotates its query tiles itself; the generic
+  // kernel reads queries rotated by the append kernel
+  if (rotary && pl.path == Path::kGeneric) {
     pl.q_rot_off = 0;
     pl.q_rot_bytes = (size_t)B * S * H * D * 2;
     pl.total_bytes = align_up(pl.q_rot_bytes, 256);
@@ -238,7 +240,7 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
       break;
     case Path::kPrefillTC:
     case Path::kGeneric: {
-      void* q_rot = cos_cache ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
+      void* q_rot = (cos_cache && pl.path == Path::kGeneric) ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
       e = launch_rope_append(a, q_rot);
       if (e == cudaSuccess)
         e = pl.path == Path::kPrefillTC ? launch_prefill_tc(a, q_rot ? q_rot : query)

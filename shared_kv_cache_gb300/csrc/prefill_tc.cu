@@ -59,8 +59,9 @@ constexpr int kQOff = 0;                   // Q_A, then Q_B
 constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKSt * kTileBytes;
 constexpr int kBarOff = kVOff + kVSt * kTileBytes;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain
-constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain,
+// q_ready
+constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1;
 constexpr int kSlotOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kSlotOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -74,8 +75,10 @@ struct PrefillParams {
   int* err;
   const int32_t* seqlens;
   const void* bias;  // [Bb, Hb, S, total] or nullptr
-  void* out;         // [B, S, H*D]
-  int B, S, H, Hkv, G, M, total, window, bias_b, bias_h, n_qt, n_pairs;
+  const void* cos;   // [rows, D/2] or nullptr: the query tiles are rotated here
+  const void* sin;
+  void* out;  // [B, S, H*D]
+  int B, S, H, Hkv, G, M, total, window, bias_b, bias_h, n_qt, n_pairs, interleaved;
   float scale_log2;
 };
 
@@ -107,6 +110,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t p_full = s_full + 16;         // [A, B]
   const uint32_t o_done = p_full + 16;         // [A, B]
   const uint32_t drain = o_done + 16;
+  const uint32_t q_ready = drain + 8;  // query tiles rotated in shared memory
+  const bool rot = p.cos != nullptr;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -150,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_done + 8 * s, 1);
     }
     mbar_init(drain, 1);
+    mbar_init(q_ready, 256);
     fence_mbar_init();
   }
   if (warp == 1) tc::alloc(smem_u32(tslot), kTmemCols);
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBN / 16; ++k) tc::mma_ts(od, pa + 64 + k * 8, vb + k * (2048 >> 4), kHi, id_o, 1u);
         tc::commit(o_done + 8 * t);
       };
-      bool ok = mbar_wait(q_full, 0, p.err) && mbar_wait(k_full, 0, p.err);
+      bool ok = mbar_wait(rot ? q_ready : q_full, 0, p.err) && mbar_wait(k_full, 0, p.err);
       if (ok) {
         tc::fence_after();
         for (int t = 0; t < ntile; ++t) issue_s(0, t);
@@ -286,6 +292,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_ref = -INFINITY, l_run = 0.f;
     const bool active = t == 0 || has_b;
     bool ok = active;
+    if (rot) {
+      // Rotary embedding of this thread's query row (position past + i) in
+      // shared memory, once the tile has landed: the rotation of the append
+      // kernel, applied to the 128-byte-swizzled tile (element j of a row
+      // sits in box j / 64, 16-byte chunk (j % 64) / 8, chunk slot
+      // chunk ^ (row % 8)).  Rows past S hold the copy's zero fill.
+      const bool do_row = active && i < p.S;
+      uint4 cq[8], sq[8];  // the position's cos and sin rows (64 values each)
+      if (do_row) {
+        const uint4* cr = reinterpret_cast<const uint4*>(static_cast<const T*>(p.cos) + (size_t)pos * (kD / 2));
+        const uint4* sr = reinterpret_cast<const uint4*>(static_cast<const T*>(p.sin) + (size_t)pos * (kD / 2));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          cq[c] = cr[c];
+          sq[c] = sr[c];
+        }
+      }
+      if (__all_sync(0xffffffffu, mbar_wait(q_full, 0, p.err)) && do_row) {
+        uint8_t* qrow = smem + kQOff + t * kQBytes + row * 128;
+        auto half8 = [](const uint4& u, int k) {  // 16-bit element k (0..7) of a 16-byte chunk
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          const float2 f = E::unpack2(w[k >> 1]);
+          return (k & 1) ? f.y : f.x;
+        };
+        if (!p.interleaved) {
+          // pairs (j, j + 64): chunk c of box 0 with chunk c of box 1
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int so = ((c ^ (row & 7)) << 4);
+            uint4* p1 = reinterpret_cast<uint4*>(qrow + so);
+            uint4* p2 = reinterpret_cast<uint4*>(qrow + kBoxBytes + so);
+            const uint4 x1 = *p1, x2 = *p2;
+            uint32_t y1[4], y2[4];
+#pragma unroll
+            for (int k = 0; k < 8; k += 2) {
+              float a0, b0, a1, b1;
+              rotate_pair(half8(x1, k), half8(x2, k), half8(cq[c], k), half8(sq[c], k), a0, b0);
+              rotate_pair(half8(x1, k + 1), half8(x2, k + 1), half8(cq[c], k + 1), half8(sq[c], k + 1), a1, b1);
+              y1[k >> 1] = E::pack2(a0, a1);
+              y2[k >> 1] = E::pack2(b0, b1);
+            }
+            *p1 = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+            *p2 = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+          }
+        } else {
+          // pairs (2j, 2j + 1) inside each chunk: chunk c of box b holds
+          // pairs j = 32 b + 4 c .. + 3
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              uint4* pc = reinterpret_cast<uint4*>(qrow + bx * kBoxBytes + ((c ^ (row & 7)) << 4));
+              const uint4 x = *pc;
+              const int j0 = 32 * bx + 4 * c;
+              uint32_t y[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int j = j0 + k;
+                float a, bb;
+                rotate_pair(half8(x, 2 * k), half8(x, 2 * k + 1), half8(cq[j >> 3], j & 7), half8(sq[j >> 3], j & 7),
+                            a, bb);
+                y[k] = E::pack2(a, bb);
+              }
+              *pc = make_uint4(y[0], y[1], y[2], y[3]);
+            }
+        }
+        fence_proxy_async_smem();  // visible to the tensor core's reads
+      }
+      mbar_arrive(q_ready);
+    }
     const float bias_unit = kLog2e / p.scale_log2;  // bias in raw score units (scale > 0)
     for (int j = 0; j < n_kv && ok; ++j) {
       const int k0 = kstart + j * kBN;
@@ -527,8 +603,9 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
   const int n_qt = (a.S + kBM - 1) / kBM;
   const int G = a.H / a.Hkv;
   const int n_pairs = (G + 1) / 2;
-  PrefillParams p{a.err, a.seqlens, a.bias, a.out, a.B, a.S, a.H, a.Hkv, G, a.M, a.total, a.window, a.bias_b,
-                  a.bias_h, n_qt, n_pairs, a.scale * kLog2e};
+  PrefillParams p{a.err,    a.seqlens, a.bias,   a.cos,  a.sin,    a.out,  a.B,          a.S,
+                  a.H,      a.Hkv,     G,        a.M,    a.total,  a.window, a.bias_b,   a.bias_h,
+                  n_qt,     n_pairs,   a.interleaved, a.scale * kLog2e};
   auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
   static bool attr_set[64][2] = {};  // per device and instantiation
   int dev = 0;

@@ -172,6 +172,11 @@ def test_decode_repeat_is_idempotent():
     dict(S=129, past=(5, 0, 300), M=512, window=100, bias=(3, 1), seed=42),
     dict(S=257, past=(0, 130, 255), M=600, window=300, dtype="bf16", seed=43),
     dict(S=128, past=(128, 0, 383), M=512, H=16, Hkv=2, seed=44),
+    # query rotation inside the tensor-core kernel: interleaved pairs, and an
+    # odd group size (the last head of each KV head runs alone)
+    dict(S=150, past=(0, 40, 300), M=512, interleaved=1, seed=45),
+    dict(S=140, past=(2, 0, 200), M=400, H=12, Hkv=4, interleaved=1, dtype="bf16", seed=46),
+    dict(S=70, past=(9, 0, 31), M=128, H=6, Hkv=2, seed=47),
 ])
 def test_prefill_cases(kw):
     check(custom(**kw))
