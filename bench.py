@@ -199,11 +199,9 @@ class Problem:
             raise RuntimeError(self.gqa.gqa_status_string(st))
 
     def launches_per_step(self):
-        # decode: the split-KV kernel, plus the combine kernel when a sequence spans splits;
-        # prefill: rotary/append kernel plus the attention kernel
-        if self.decode:
-            return 2 if self.ws_bytes > 0 else 1
-        return 2
+        # decode: one kernel (append, split-KV attention and the split combine);
+        # prefill: the rotary/append kernel plus the attention kernel
+        return 1 if self.decode else 2
 
 
 def time_steps(prob, steps, warmup, stream, ws_count=1, device=None):
@@ -321,8 +319,6 @@ print(json.dumps({{"value": nbytes * n / dt / 1e9, "calls": n, "seconds": dt, "s
 # kernel per launch, from the ncu captures summarised in profiles/; a kernel
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
-    "decode_b16": 105336832 + 3085312,     # decode_kernel, profiles/decode_kernel_decode_b16.md
-    "prefill_2k": 102152704 + 31195136,    # prefill_kernel, profiles/prefill_kernel_prefill_2k.md
 }
 
 
@@ -377,11 +373,11 @@ def run_ours(args):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     if prob.decode:
-        roofline = {"kernel": "decode_kernel + combine_kernel (one gqa_forward call)", "bound": "hbm",
+        roofline = {"kernel": "decode_dyn_kernel (one gqa_forward call)", "bound": "hbm",
                     "achieved": rate, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": rate / pk["hbm_gbs"],
                     "peak_source": pk["source"], "frac_of_nominal_8tbs": rate / 8000.0,
                     "bytes_per_launch": prob.bytes, "traffic": TRAFFIC.get(name),
-                    "traffic_kernel": "decode_kernel"}
+                    "traffic_kernel": "decode_dyn_kernel"}
     else:
         roofline = {"kernel": "rope_append_kernel + prefill_kernel (one gqa_forward call)", "bound": "tensor",
                     "achieved": rate, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",

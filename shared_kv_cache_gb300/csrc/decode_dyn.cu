@@ -1,0 +1,980 @@
+// Split-KV flash-decode for one new token per sequence (S = 1), D = 128, with
+// dynamic work distribution and the split combine done inside the kernel.
+//
+// Work decomposition.  The keys each (sequence b, KV head kh) item must scan
+// run from the window start lo_b to the true length L_b = past_b + 1; the scan
+// stops there and never sweeps max_seq_len ("KV Cache", rocMLIR discussion,
+// "Short summary of notes").  Those keys are cut into 64-key tiles, and each
+// item's tiles into chunks of C tiles, C chosen so that there are about
+// chunks_per_cta chunks per CTA of the persistent grid (about two CTAs per
+// SM).  CTA c starts on chunk c; every further chunk is handed out by an
+// atomic ticket, so CTAs that the memory system serves faster take more
+// chunks and all of them finish together.
+//
+// Split combine.  An item cut into n > 1 chunks leaves one fp32 partial
+// (o, m, l) per chunk, m the running max in log2 units.  Each chunk's CTA
+// writes its partial and counts itself in on the item's arrival counter; the
+// last of the n merges them,
+//   m* = max_k m_k,  o = sum_k 2^(m_k - m*) o_k / sum_k 2^(m_k - m*) l_k,
+// and writes the output row.  Items of one chunk write their row directly.
+//
+// The two counters live in the caller's workspace, whose contents on entry
+// are arbitrary, so each is a 64-bit word (epoch, count) keyed to a per-call
+// epoch: the first user of a stale word installs the current epoch, and the
+// last user puts it back to zero.
+//
+// Inside a CTA.  Warp 4 is the producer: it computes the partition from
+// seqlens_k, takes chunks, and for each one hands the consumers a descriptor
+// with the chunk's query rows, cos/sin rows and (for the item's last chunk)
+// the new K/V rows, fetched by bulk copies into a two-slot staging area; then
+// it streams [64 keys x 128] K and V tiles into a 3-stage ring with 2-D
+// bulk-tensor copies (TMA, 128-byte swizzle).  Warps 0..3 each own 16 keys of
+// every tile and run S^T = K Q^T and O^T += V^T P^T with mma.sync m16n8k16,
+// the G query heads of the group as the 8-wide N dimension, so every K/V tile
+// loaded is reused by the whole group.
+//
+// Fused steps.  Each chunk rotates its G query rows at position past_b; the
+// CTA whose chunk holds an item's last tile also rotates the new key row,
+// appends the new K/V row at slot past_b ("[TorchOnnxToTorch] Add pad+scatter
+// KV cache and mask to GQA", PR description: rotary at arange + past length,
+// scatter at seqlens_k) and patches that row into the shared-memory tile, so
+// the TMA load never has to observe the global write.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gqa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = kDecodeTile;           // keys per stage
+constexpr int kCW = 4;                       // consumer warps (16 keys each)
+constexpr int kStages = 3;
+constexpr int kThreads = (kCW + 2) * 32;  // consumers, producer, merger
+constexpr int kProducer = kCW, kMerger = kCW + 1;  // warp indices
+constexpr int kBoxBytes = kTile * 128;       // one 64-column box of a tile
+constexpr int kTileBytes = 2 * kBoxBytes;    // K (or V) tile, 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;  // K + V
+constexpr int kQStride = kD + 8;             // padded query row (elements)
+constexpr int kRing = kStages * kStageBytes;
+constexpr int kSlots = 2;                    // descriptor / staging slots
+constexpr int kMail = 4;                     // consumer -> merger mailbox entries
+constexpr size_t kSmPerSM = 233472;          // shared memory per SM (bytes)
+constexpr size_t kSmReservedPerCta = 1024;
+constexpr int kSeqCache = 128;               // seqlens_k entries cached in shared memory
+
+// Descriptor of one chunk, written by the producer into a staging slot.
+struct ChunkDesc {
+  int u;           // chunk index, -1: no more chunks
+  int b, kh;       // item
+  int t0, t1, tb;  // tile range [t0, t1) of the item's tb tiles
+  int klo, L;      // keys [klo, L) of the item
+  int slot;        // partial slot of this chunk, -1: the item is one chunk
+  int first_slot;  // the item's first partial slot (its arrival counter)
+  int n;           // chunks of the item
+  int pad[5];
+};
+static_assert(sizeof(ChunkDesc) == 64, "descriptor size");
+
+// Shared-memory layout after the ring, for group size G.
+struct Layout {
+  int merge_warp_bytes;  // one warp's (O^T, m, l) hand-off
+  int merge_off;         // merge region: two hand-off slots (also holds the rotated query rows)
+  int slot_bytes;        // one staging slot: descriptor, q rows, cos, sin, new K, new V rows
+  int slot_off;
+  int new_off;           // rotated new K row then V row
+  int seq_off;           // seqlens_k cache (kSeqCache entries)
+  int mail_off;          // consumer -> merger mailbox (kMail entries of 4 ints)
+  int bar_off;
+  int total;             // bytes, including 1 KB of alignment slack
+};
+__host__ __device__ constexpr Layout layout_for(int G) {
+  const int nt = G <= 8 ? 1 : 2;                        // 8-head column tiles
+  const int w = nt * (8 * 4 * 32 * 4 + 4 * 32 * 4);     // O^T fragments + (m, l) pairs, per lane
+  int merge = 2 * w;
+  const int qbytes = 16 * kQStride * 2;
+  if (merge < qbytes) merge = qbytes;
+  const int merge_off = kRing;
+  const int slot_bytes = (64 + G * kD * 2 + 2 * 128 + 2 * 256 + 127) / 128 * 128;
+  const int slot_off = merge_off + merge;
+  const int new_off = slot_off + kSlots * slot_bytes;
+  const int seq_off = new_off + 2 * kD * 2;
+  const int mail_off = seq_off + kSeqCache * 4;
+  const int bar_off = mail_off + kMail * 16;
+  return Layout{w, merge_off, slot_bytes, slot_off, new_off, seq_off, mail_off, bar_off,
+                bar_off + (2 * kStages + 2 * kSlots + 2 * kMail) * 8 + 1024};
+}
+// staging offsets inside a slot
+__host__ __device__ constexpr int st_q() { return 64; }
+__host__ __device__ constexpr int st_cos(int G) { return 64 + G * kD * 2; }
+__host__ __device__ constexpr int st_sin(int G) { return st_cos(G) + 128; }
+__host__ __device__ constexpr int st_kn(int G) { return st_sin(G) + 128; }
+__host__ __device__ constexpr int st_vn(int G) { return st_kn(G) + 256; }
+
+struct DynParams {
+  const void* q;     // [B, 1, H*D]
+  const void* knew;  // [B, 1, Hkv*D]
+  const void* vnew;
+  void* kbuf;  // [B, Hkv, M, D]
+  void* vbuf;
+  const int32_t* seqlens;
+  const void* cos;  // [rows, D/2] or nullptr
+  const void* sin;
+  const void* bias;  // [Bb, Hb, 1, total] or nullptr
+  void* out;         // [B, 1, H*D]
+  float* part_o;     // [slots][G][D]
+  float* part_ml;    // [slots][G][2]
+  unsigned long long* ticket;    // chunk ticket (epoch, count)
+  unsigned long long* arrivals;  // [slots] per-item arrival counters (epoch, count), at the item's first slot
+  int* err;
+  int B, H, Hkv, G, M, total, window, P, interleaved, bias_b, bias_h, chunks_per_cta;
+  uint32_t epoch;
+  float scale_log2;
+};
+
+// Byte offset of 16-byte chunk c (0..15) of row r inside a [kTile x 128]
+// tile held as two 128-byte-wide boxes, each with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+  return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Keys of sequence b: [lo, L); returns its tile count (0 when the sequence
+// fails the length check and is skipped).
+__device__ __forceinline__ int seq_tiles(const DynParams& p, int past, int& lo, int& L) {
+  if (sequence_error(past, 1, p.M, p.total)) {
+    lo = L = 0;
+    return 0;
+  }
+  L = past + 1;
+  lo = p.window > 0 ? max(0, L - p.window) : 0;
+  return (L - lo + kTile - 1) / kTile;
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// (epoch, count) counters.  Before its first count in a call, a user makes
+// sure the word holds this call's epoch: it reads the word and, if the word
+// holds another epoch (left by an earlier call, or never initialised),
+// replaces exactly that value by (epoch, 0) -- one compare-and-swap, which
+// fails harmlessly when another user has installed the epoch first.  Counts
+// are then plain atomic additions.  The last user of the call resets the
+// word to 0, before which every user has made its installation attempt.
+__device__ __forceinline__ void epoch_install(unsigned long long* c, uint32_t epoch) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(c) : "memory");
+  if ((uint32_t)(v >> 32) != epoch) atomicCAS(c, v, (unsigned long long)epoch << 32);
+}
+// Returns the count before this one, or 0xFFFFFFFF (recorded as a device
+// error) if the word does not hold this call's epoch.
+__device__ __forceinline__ uint32_t epoch_take(unsigned long long* c, uint32_t epoch, int* err) {
+  const unsigned long long old = atomicAdd(c, 1ull);
+  if ((uint32_t)(old >> 32) != epoch) {
+    record_error(err, GQA_ERR_INVALID_ARGUMENT);  // the workspace changed under the call
+    return 0xFFFFFFFFu;
+  }
+  return (uint32_t)old;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// The partition, computed identically by every producer warp: per-sequence
+// tile counts, the chunk size C and the chunk count U.
+struct Partition {
+  int C, U;
+};
+__device__ Partition make_partition(const DynParams& p, const int* sl, int lane) {
+  int T = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int lo, L;
+    const int b = b0 + lane;
+    T += warp_sum(b < p.B ? seq_tiles(p, sl[b], lo, L) : 0);
+  }
+  T *= p.Hkv;
+  const int target = p.chunks_per_cta * p.P;
+  const int C = max(2, (T + target - 1) / target);
+  int U = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int lo, L;
+    const int b = b0 + lane;
+    const int tb = b < p.B ? seq_tiles(p, sl[b], lo, L) : 0;
+    U += warp_sum((tb + C - 1) / C);
+  }
+  return Partition{C, U * p.Hkv};
+}
+
+// Warp-cooperative: the item and tile range of chunk u (< U).
+__device__ ChunkDesc locate_chunk(const DynParams& p, const int* sl, const Partition& pt, int u, int lane) {
+  int cbase = 0, sbase = 0;  // chunks and partial slots of the sequences before b0
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    int lo, L;
+    const int b = b0 + lane;
+    const int tb = b < p.B ? seq_tiles(p, sl[b], lo, L) : 0;
+    const int nb = (tb + pt.C - 1) / pt.C;
+    const int ch = nb * p.Hkv;
+    const int sl_n = nb > 1 ? ch : 0;
+    const int incl = warp_incl_scan(ch, lane);
+    const int sincl = warp_incl_scan(sl_n, lane);
+    const int chunk_total = __shfl_sync(0xffffffffu, incl, 31);
+    if (u < cbase + chunk_total) {
+      const unsigned m = __ballot_sync(0xffffffffu, cbase + incl > u);
+      const int l = __ffs(m) - 1;
+      ChunkDesc d;
+      d.b = b0 + l;
+      const int c0 = cbase + __shfl_sync(0xffffffffu, incl - ch, l);
+      const int s0 = sbase + __shfl_sync(0xffffffffu, sincl - sl_n, l);
+      d.tb = __shfl_sync(0xffffffffu, tb, l);
+      d.klo = __shfl_sync(0xffffffffu, lo, l);
+      d.L = __shfl_sync(0xffffffffu, L, l);
+      d.n = __shfl_sync(0xffffffffu, nb, l);
+      const int r = u - c0;
+      d.kh = r / d.n;
+      const int k = r - d.kh * d.n;
+      d.t0 = k * pt.C;
+      d.t1 = min(d.t0 + pt.C, d.tb);
+      d.u = u;
+      d.first_slot = d.n > 1 ? s0 + d.kh * d.n : -1;
+      d.slot = d.n > 1 ? d.first_slot + k : -1;
+      return d;
+    }
+    cbase += chunk_total;
+    sbase += __shfl_sync(0xffffffffu, sincl, 31);
+  }
+  ChunkDesc d{};
+  d.u = -1;
+  return d;
+}
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_dyn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const DynParams p) {
+  using E = Elem<T>;
+  constexpr bool kBF16 = E::is_bf16;
+  const int G = p.G;
+  const Layout lay = layout_for(G);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  T* qs = reinterpret_cast<T*>(smem + lay.merge_off);  // rotated query rows (aliases the merge region)
+  T* news = reinterpret_cast<T*>(smem + lay.new_off);
+  const uint32_t bar_full = sbase + lay.bar_off;
+  const uint32_t bar_empty = bar_full + kStages * 8;
+  const uint32_t bar_dfull = bar_empty + kStages * 8;
+  const uint32_t bar_dempty = bar_dfull + kSlots * 8;
+  const uint32_t bar_mfull = bar_dempty + kSlots * 8;  // mailbox to the merger warp
+  const uint32_t bar_mempty = bar_mfull + kMail * 8;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(bar_full + 8 * i, 1);
+      mbar_init(bar_empty + 8 * i, kCW);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar_dfull + 8 * i, 1);
+      mbar_init(bar_dempty + 8 * i, kCW);
+    }
+    for (int i = 0; i < kMail; ++i) {
+      mbar_init(bar_mfull + 8 * i, 1);
+      mbar_init(bar_mempty + 8 * i, 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == kProducer && lane == 0) {
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  // inputs may be written by the previous kernel in the stream
+  pdl_wait_primary();
+
+  if (warp == kProducer) {
+    // ---------------- producer ----------------
+    int* s_seq = reinterpret_cast<int*>(smem + lay.seq_off);
+    const bool cached = p.B <= kSeqCache;
+    if (cached)
+      for (int i = lane; i < p.B; i += 32) s_seq[i] = p.seqlens[i];
+    __syncwarp();
+    const int* sl = cached ? s_seq : p.seqlens;
+    if (c == 0)  // sequences that fail the length check are skipped and reported once
+      for (int i = lane; i < p.B; i += 32) {
+        const int e = sequence_error(sl[i], 1, p.M, p.total);
+        if (e) record_error(p.err, e);
+      }
+    const Partition pt = make_partition(p, sl, lane);
+    const bool rot = p.cos != nullptr;
+    int u = c < pt.U ? c : -1;
+    int gt = 0;  // tiles issued by this CTA
+    int dk = 0;  // descriptors issued
+    bool ok = true;
+    bool first_take = true;
+    while (true) {
+      ChunkDesc d;
+      if (u >= 0) {
+        d = locate_chunk(p, sl, pt, u, lane);
+      } else {
+        d = ChunkDesc{};
+        d.u = -1;
+      }
+      // descriptor slot (free once the consumers have read the chunk two back)
+      const int ds = dk % kSlots;
+      if (dk >= kSlots && !mbar_wait(bar_dempty + 8 * ds, ((dk / kSlots) - 1) & 1, p.err)) ok = false;
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) d.u = -1;  // a wait ran out: stop the consumers
+      const uint32_t slot = sbase + lay.slot_off + ds * lay.slot_bytes;
+      const bool has_new = d.u >= 0 && d.t1 == d.tb;
+      if (lane == 0) {
+        *reinterpret_cast<ChunkDesc*>(smem + lay.slot_off + ds * lay.slot_bytes) = d;
+        if (d.u >= 0 && ok) {
+          const uint32_t bytes = G * kD * 2 + (rot ? 256u : 0u) + (has_new ? 512u : 0u);
+          const uint32_t fb = bar_dfull + 8 * ds;
+          mbar_arrive_expect_tx(fb, bytes);
+          bulk_g2s(slot + st_q(), static_cast<const T*>(p.q) + ((size_t)d.b * p.H + (size_t)d.kh * G) * kD,
+                   G * kD * 2, fb);
+          if (rot) {
+            const size_t crow = (size_t)(d.L - 1) * (kD / 2);
+            bulk_g2s(slot + st_cos(G), static_cast<const T*>(p.cos) + crow, 128, fb);
+            bulk_g2s(slot + st_sin(G), static_cast<const T*>(p.sin) + crow, 128, fb);
+          }
+          if (has_new) {
+            const size_t row = ((size_t)d.b * p.Hkv + d.kh) * kD;
+            bulk_g2s(slot + st_kn(G), static_cast<const T*>(p.knew) + row, 256, fb);
+            bulk_g2s(slot + st_vn(G), static_cast<const T*>(p.vnew) + row, 256, fb);
+          }
+        } else {
+          mbar_arrive(bar_dfull + 8 * ds);  // the terminating descriptor (u = -1)
+        }
+      }
+      ++dk;
+      if (d.u < 0 || !ok) break;
+      if (lane == 0) {
+        const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo;
+        for (int t = d.t0; t < d.t1; ++t, ++gt) {
+          const int st = gt % kStages;
+          const int round = gt / kStages;
+          if (round > 0 && !mbar_wait(bar_empty + 8 * st, (round - 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_full + 8 * st;
+          const uint32_t kd = sbase + st * kStageBytes;
+          const uint32_t vd = kd + kTileBytes;
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          const int y = row0 + t * kTile;
+          tma_load_2d(kd, &kmap, 0, y, fb);
+          tma_load_2d(kd + kBoxBytes, &kmap, 64, y, fb);
+          tma_load_2d(vd, &vmap, 0, y, fb);
+          tma_load_2d(vd + kBoxBytes, &vmap, 64, y, fb);
+        }
+      }
+      gt = __shfl_sync(0xffffffffu, gt, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // the next chunk's ticket (its latency hides behind the tiles queued in
+      // the ring); the call's last ticket resets the counter
+      int nu = -1;
+      if (lane == 0 && ok) {
+        if (first_take) {
+          epoch_install(p.ticket, p.epoch);
+          first_take = false;
+        }
+        const uint32_t t = epoch_take(p.ticket, p.epoch, p.err);
+        if (t != 0xFFFFFFFFu) {
+          if ((int)t == pt.U - 1) atomicExch(p.ticket, 0ull);
+          nu = p.P + (int)t < pt.U ? p.P + (int)t : -1;
+        }
+      }
+      u = __shfl_sync(0xffffffffu, nu, 0);
+    }
+    // Leave no copy in flight into this CTA's shared memory (after a
+    // timeout the consumers may not have waited for every tile).
+    if (lane == 0) {
+      for (int t = max(0, gt - kStages); t < gt; ++t)
+        mbar_wait(bar_full + 8 * (t % kStages), (t / kStages) & 1, p.err);
+      for (int k = max(0, dk - kSlots); k < dk; ++k)
+        mbar_wait(bar_dfull + 8 * (k % kSlots), (k / kSlots) & 1, p.err);
+    }
+    return;
+  }
+
+  if (warp == kMerger) {
+    // ---------------- merger ----------------
+    // Counts each finished partial in on its item's arrival counter and, for
+    // the item's last chunk, merges the item's partials into its output row,
+    // off the consumers' path.
+    int mk = 0;
+    while (true) {
+      const int ms = mk % kMail;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_mfull + 8 * ms, (mk / kMail) & 1, p.err))) break;
+      const int* mail = reinterpret_cast<const int*>(smem + lay.mail_off + ms * 16);
+      const int first = mail[0], n = mail[1], b = mail[2], kh = mail[3];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_mempty + 8 * ms);
+      ++mk;
+      if (first < 0) break;  // the consumers are done
+      unsigned long long* arr = p.arrivals + first;
+      uint32_t cnt = 0;
+      if (lane == 0) {
+        // the partial, written by consumer warp 0 before the mailbox handed
+        // it over (CTA scope), is made visible at GPU scope before the count
+        __threadfence();
+        epoch_install(arr, p.epoch);
+        cnt = epoch_take(arr, p.epoch, p.err);
+      }
+      cnt = __shfl_sync(0xffffffffu, cnt, 0);
+      if (cnt != (uint32_t)(n - 1)) continue;
+      // the item's last chunk: merge its n partials (read through L2)
+      __threadfence();
+      T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
+      const float* ml0 = p.part_ml + (size_t)first * G * 2;
+      const float* po0 = p.part_o + (size_t)first * G * kD;
+      // heads four at a time; the loads of a round are independent, so a
+      // merge costs about n / 32 + n / 4 round trips to L2 per head group
+      const int d4 = lane * 4;
+      for (int g0 = 0; g0 < G; g0 += 4) {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int k = lane; k < n; k += 32) {
+#pragma unroll
+          for (int gi = 0; gi < 4; ++gi)
+            if (g0 + gi < G) mx[gi] = fmaxf(mx[gi], __ldcg(ml0 + ((size_t)k * G + g0 + gi) * 2));
+        }
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx[gi] = fmaxf(mx[gi], __shfl_xor_sync(0xffffffffu, mx[gi], o));
+          if (mx[gi] == -INFINITY) mx[gi] = 0.f;
+        }
+        float4 acc[4];
+        float l[4];
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) acc[gi] = make_float4(0.f, 0.f, 0.f, 0.f), l[gi] = 0.f;
+        for (int k0 = 0; k0 < n; k0 += 4) {
+          float4 ov[4][4];
+          float2 mlv[4][4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) {
+              const int k = k0 + q, g = g0 + gi;
+              const bool v = k < n && g < G;
+              ov[q][gi] = v ? __ldcg(reinterpret_cast<const float4*>(po0 + ((size_t)k * G + g) * kD + d4))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+              mlv[q][gi] = v ? __ldcg(reinterpret_cast<const float2*>(ml0 + ((size_t)k * G + g) * 2))
+                             : make_float2(-INFINITY, 0.f);
+            }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) {
+              const float w = fast_exp2(mlv[q][gi].x - mx[gi]);
+              l[gi] += w * mlv[q][gi].y;
+              acc[gi].x += w * ov[q][gi].x;
+              acc[gi].y += w * ov[q][gi].y;
+              acc[gi].z += w * ov[q][gi].z;
+              acc[gi].w += w * ov[q][gi].w;
+            }
+        }
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          if (g0 + gi >= G) continue;
+          const float inv = 1.f / l[gi];
+          uint2 packed;
+          packed.x = E::pack2(acc[gi].x * inv, acc[gi].y * inv);
+          packed.y = E::pack2(acc[gi].z * inv, acc[gi].w * inv);
+          *reinterpret_cast<uint2*>(outg + (size_t)(g0 + gi) * kD + d4) = packed;
+        }
+      }
+      if (lane == 0) atomicExch(arr, 0ull);  // ready for the next call
+    }
+    return;
+  }
+
+  // ---------------- consumers (warps 0..3, 128 threads) ----------------
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row / column group
+  const bool rot = p.cos != nullptr;
+  const bool inter = p.interleaved != 0;
+  int gt = 0;  // tiles consumed by this CTA
+  int dk = 0;  // descriptors consumed
+  int mk = 0;  // partials handed to the merger (warp 0)
+  while (true) {
+    const int ds = dk % kSlots;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar_dfull + 8 * ds, (dk / kSlots) & 1, p.err))) break;
+    const uint8_t* slot = smem + lay.slot_off + ds * lay.slot_bytes;
+    const ChunkDesc d = *reinterpret_cast<const ChunkDesc*>(slot);
+    if (d.u < 0) break;
+    ++dk;
+    const int b = d.b, kh = d.kh, klo = d.klo, L = d.L, tb = d.tb;
+    const int t0 = d.t0, t1 = d.t1;
+    const int past = L - 1;
+    const bool has_new = t1 == tb;         // the item's last tile (holding key `past`) is here
+    const bool splitp = (L - klo) <= 256;  // short items: keep P at fp32-level accuracy
+    const T* st_qp = reinterpret_cast<const T*>(slot + st_q());
+    const T* st_c = reinterpret_cast<const T*>(slot + st_cos(G));
+    const T* st_s = reinterpret_cast<const T*>(slot + st_sin(G));
+    const T* st_k = reinterpret_cast<const T*>(slot + st_kn(G));
+    const T* st_v = reinterpret_cast<const T*>(slot + st_vn(G));
+
+    // -- query rows of the group rotated at position `past` (rows >= G are
+    //    zero), from the staging slot
+    named_bar_sync(1, kCW * 32);  // the previous chunk's merge reads are done
+    {
+      using V8 = VecT<T, 8>;
+      const int g = tid >> 3, j0 = (tid & 7) * 8;
+      auto rotate8 = [&](const T* src, V8& y1, V8& y2) {
+        V8 x1, x2;
+        if (!inter) {
+          x1 = *reinterpret_cast<const V8*>(src + j0);
+          x2 = *reinterpret_cast<const V8*>(src + kD / 2 + j0);
+        } else {
+          const V8 xa = *reinterpret_cast<const V8*>(src + 2 * j0);
+          const V8 xb = *reinterpret_cast<const V8*>(src + 2 * j0 + 8);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x1.v[e] = xa.v[2 * e];
+            x2.v[e] = xa.v[2 * e + 1];
+            x1.v[e + 4] = xb.v[2 * e];
+            x2.v[e + 4] = xb.v[2 * e + 1];
+          }
+        }
+        if (rot) {
+          const V8 cv = *reinterpret_cast<const V8*>(st_c + j0);
+          const V8 sv = *reinterpret_cast<const V8*>(st_s + j0);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float a, cc;
+            rotate_pair(E::to_f(x1.v[e]), E::to_f(x2.v[e]), E::to_f(cv.v[e]), E::to_f(sv.v[e]), a, cc);
+            y1.v[e] = E::from_f(a);
+            y2.v[e] = E::from_f(cc);
+          }
+        } else {
+          y1 = x1;
+          y2 = x2;
+        }
+      };
+      auto store8 = [&](T* dst, const V8& y1, const V8& y2) {
+        if (!inter) {
+          *reinterpret_cast<V8*>(dst + j0) = y1;
+          *reinterpret_cast<V8*>(dst + kD / 2 + j0) = y2;
+        } else {
+          V8 ya, yb;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ya.v[2 * e] = y1.v[e];
+            ya.v[2 * e + 1] = y2.v[e];
+            yb.v[2 * e] = y1.v[e + 4];
+            yb.v[2 * e + 1] = y2.v[e + 4];
+          }
+          *reinterpret_cast<V8*>(dst + 2 * j0) = ya;
+          *reinterpret_cast<V8*>(dst + 2 * j0 + 8) = yb;
+        }
+      };
+      for (int gg = g; gg < 8 * NT; gg += 16) {
+        V8 y1, y2;
+        if (gg < G) {
+          rotate8(st_qp + gg * kD, y1, y2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y1.v[e] = y2.v[e] = E::from_f(0.f);
+        }
+        store8(qs + gg * kQStride, y1, y2);
+      }
+      if (has_new) {
+        // the append: rotated new key row and raw value row into slot `past`
+        const size_t row = (((size_t)b * p.Hkv + kh) * p.M + past) * kD;
+        if (tid < 8) {
+          V8 k1, k2;
+          rotate8(st_k, k1, k2);
+          store8(news, k1, k2);
+          store8(static_cast<T*>(p.kbuf) + row, k1, k2);
+        } else if (tid < 24) {
+          const int dd = (tid - 8) * 8;
+          const V8 vv = *reinterpret_cast<const V8*>(st_v + dd);
+          *reinterpret_cast<V8*>(news + kD + dd) = vv;
+          *reinterpret_cast<V8*>(static_cast<T*>(p.vbuf) + row + dd) = vv;
+        }
+      }
+    }
+    named_bar_sync(1, kCW * 32);  // rotated rows ready; the staging slot is free
+    if (lane == 0) mbar_arrive(bar_dempty + 8 * ds);
+
+    // bias rows of this thread's heads (8*nt + 2*tq + e)
+    const T* brow[NT][2];
+    {
+      const int bb = p.bias_b > 1 ? b : 0;
+      const T* bbase = p.bias ? static_cast<const T*>(p.bias) + (size_t)bb * p.bias_h * p.total : nullptr;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int hd = 8 * nt + 2 * tq + e;
+          brow[nt][e] = (bbase && hd < G) ? bbase + (size_t)(p.bias_h > 1 ? kh * G + hd : 0) * p.total : nullptr;
+        }
+    }
+    // query B-fragments (d x heads), kept in registers for the whole chunk
+    uint32_t qb[NT][8][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const uint32_t qrow = smem_u32(qs + (8 * nt + (lane & 7)) * kQStride);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ldsm_x4(qrow + (4 * j + (lane >> 3)) * 16, qb[nt][2 * j][0], qb[nt][2 * j][1], qb[nt][2 * j + 1][0],
+                qb[nt][2 * j + 1][1]);
+    }
+
+    // O^T accumulators: d-tile md (rows d = 16 md + gq, +8) x heads (2 tq, 2 tq + 1)
+    float o[NT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
+    float mh[NT][2], lh[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mh[nt][0] = mh[nt][1] = -INFINITY, lh[nt][0] = lh[nt][1] = 0.f;
+
+    bool ok = true;
+    for (int t = t0; t < t1; ++t, ++gt) {
+      const int st = gt % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8 * st, (gt / kStages) & 1, p.err))) {
+        ok = false;  // the whole warp leaves together
+        break;
+      }
+      const uint32_t kst = sbase + st * kStageBytes;
+      const uint32_t vst = kst + kTileBytes;
+      const int tk0 = klo + t * kTile;  // first key of the tile
+      const int wr0 = warp * 16;        // first tile row of this warp
+      bool touched = false;
+      if (has_new && t == tb - 1) {
+        const int r = past - tk0;
+        if ((r >> 4) == warp) {
+          const int cch = lane & 15;
+          const uint4 val = *reinterpret_cast<const uint4*>(news + (lane < 16 ? 0 : kD) + cch * 8);
+          *reinterpret_cast<uint4*>(smem + ((lane < 16 ? kst : vst) - sbase + sw_off(r, cch))) = val;
+          touched = true;
+        }
+      }
+      if (tk0 + wr0 + 16 > L) {
+        // value rows beyond the length: zero them, so that P = 0 meets finite V
+        const int rz = max(L - tk0, wr0);
+        const int n = (wr0 + 16 - rz) * 16;
+        for (int idx = lane; idx < n; idx += 32)
+          *reinterpret_cast<uint4*>(smem + (vst - sbase) + sw_off(rz + (idx >> 4), idx & 15)) =
+              make_uint4(0, 0, 0, 0);
+        touched = true;
+      }
+      __syncwarp();
+
+      // S^T = K Q^T: 16 keys (rows) x 8 heads (columns) per n-tile
+      float sc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      {
+        const int mi = lane >> 3;
+        const int kr = wr0 + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(kst + sw_off(kr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816<kBF16>(sc[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+        }
+      }
+      // scale, bias, mask; the thread's keys are gq and gq + 8 of the warp's 16
+      const int key0 = tk0 + wr0 + gq;
+      uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = key0 + (e >> 1) * 8;
+          float v = sc[nt][e] * p.scale_log2;
+          const T* br = brow[nt][e & 1];
+          if (br && key < L) v = fmaf(E::to_f(br[key]), kLog2e, v);
+          sc[nt][e] = key < L ? v : -INFINITY;
+        }
+        float mx[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float m = fmaxf(sc[nt][e], sc[nt][e + 2]);
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          const float mn = fmaxf(mh[nt][e], m);
+          const float mu = mn == -INFINITY ? 0.f : mn;
+          mx[e] = mu;
+          const float corr = fast_exp2(mh[nt][e] - mu);
+          mh[nt][e] = mn;
+          lh[nt][e] *= corr;
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            o[nt][md][e] *= corr;
+            o[nt][md][e + 2] *= corr;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = fast_exp2(sc[nt][e] - mx[e & 1]);
+        lh[nt][0] += sc[nt][0] + sc[nt][2];
+        lh[nt][1] += sc[nt][1] + sc[nt][3];
+        // P^T (keys x heads) -> B fragments: transpose the two 8x8 halves.
+        // Short items also carry P's rounding residue (P = hi + lo, both
+        // 16-bit), so that P.V keeps fp32-level accuracy where a few keys
+        // dominate the output.
+        const uint32_t h0 = E::pack2(sc[nt][0], sc[nt][1]);
+        const uint32_t h1 = E::pack2(sc[nt][2], sc[nt][3]);
+        bh[nt][0] = movmatrix_trans(h0);
+        bh[nt][1] = movmatrix_trans(h1);
+        if (splitp) {
+          const float2 f0 = E::unpack2(h0), f1 = E::unpack2(h1);
+          bl[nt][0] = movmatrix_trans(E::pack2(sc[nt][0] - f0.x, sc[nt][1] - f0.y));
+          bl[nt][1] = movmatrix_trans(E::pack2(sc[nt][2] - f1.x, sc[nt][3] - f1.y));
+        }
+      }
+      // O^T += V^T P^T over this warp's 16 keys
+      {
+        const int mi = lane >> 3;
+        const int vr = wr0 + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          uint32_t a[4];
+          ldsm_x4_t(vst + sw_off(vr, 2 * md + (mi & 1)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_16816<kBF16>(o[nt][md], a, bh[nt][0], bh[nt][1]);
+            if (splitp) mma_16816<kBF16>(o[nt][md], a, bl[nt][0], bl[nt][1]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (touched) fence_proxy_async_smem();
+        mbar_arrive(bar_empty + 8 * st);
+      }
+    }
+
+    // -- merge the four warps' (O^T, m, l) in two rounds through shared memory
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float l = lh[nt][e];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        lh[nt][e] = l;
+      }
+    // every warp is done reading the ring and the query rows; leave together
+    // if any wait ran out
+    if (!named_bar_and(1, kCW * 32, ok)) break;
+    float* mw = reinterpret_cast<float*>(smem + lay.merge_off);
+    const int wfl = lay.merge_warp_bytes / 4;  // floats per hand-off slot
+    auto hand_off = [&](float* dst) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int md = 0; md < 8; ++md)
+          *reinterpret_cast<float4*>(dst + ((nt * 8 + md) * 32 + lane) * 4) =
+              make_float4(o[nt][md][0], o[nt][md][1], o[nt][md][2], o[nt][md][3]);
+        *reinterpret_cast<float4*>(dst + NT * 8 * 128 + (nt * 32 + lane) * 4) =
+            make_float4(mh[nt][0], lh[nt][0], mh[nt][1], lh[nt][1]);
+      }
+    };
+    auto absorb = [&](const float* src) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float4 ml = *reinterpret_cast<const float4*>(src + NT * 8 * 128 + (nt * 32 + lane) * 4);
+        float f1[2], f2[2];
+        const float m2[2] = {ml.x, ml.z}, l2[2] = {ml.y, ml.w};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float ms = fmaxf(mh[nt][e], m2[e]);
+          const float su = ms == -INFINITY ? 0.f : ms;
+          f1[e] = fast_exp2(mh[nt][e] - su);
+          f2[e] = fast_exp2(m2[e] - su);
+          lh[nt][e] = lh[nt][e] * f1[e] + l2[e] * f2[e];
+          mh[nt][e] = ms;
+        }
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          const float4 a = *reinterpret_cast<const float4*>(src + ((nt * 8 + md) * 32 + lane) * 4);
+          o[nt][md][0] = o[nt][md][0] * f1[0] + a.x * f2[0];
+          o[nt][md][1] = o[nt][md][1] * f1[1] + a.y * f2[1];
+          o[nt][md][2] = o[nt][md][2] * f1[0] + a.z * f2[0];
+          o[nt][md][3] = o[nt][md][3] * f1[1] + a.w * f2[1];
+        }
+      }
+    };
+    if (warp >= 2) hand_off(mw + (warp - 2) * wfl);
+    named_bar_sync(1, kCW * 32);
+    if (warp < 2) absorb(mw + warp * wfl);
+    named_bar_sync(1, kCW * 32);
+    if (warp == 1) hand_off(mw);
+    named_bar_sync(1, kCW * 32);
+    if (warp == 0) {
+      absorb(mw);
+      T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
+      if (d.slot < 0) {
+        // the item is this one chunk: its output row
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int hd0 = 8 * nt + 2 * tq;  // this thread's heads: hd0, hd0 + 1
+          const float i0 = 1.f / lh[nt][0], i1 = 1.f / lh[nt][1];
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            const int dd = 16 * md + gq;
+            if (hd0 < G) {
+              outg[(size_t)hd0 * kD + dd] = E::from_f(o[nt][md][0] * i0);
+              outg[(size_t)hd0 * kD + dd + 8] = E::from_f(o[nt][md][2] * i0);
+            }
+            if (hd0 + 1 < G) {
+              outg[(size_t)(hd0 + 1) * kD + dd] = E::from_f(o[nt][md][1] * i1);
+              outg[(size_t)(hd0 + 1) * kD + dd + 8] = E::from_f(o[nt][md][3] * i1);
+            }
+          }
+        }
+      } else {
+        // this chunk's partial, then the item's arrival count
+        float* po = p.part_o + (size_t)d.slot * G * kD;
+        float* pm = p.part_ml + (size_t)d.slot * G * 2;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int hd0 = 8 * nt + 2 * tq;
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            const int dd = 16 * md + gq;
+            if (hd0 < G) {
+              po[(size_t)hd0 * kD + dd] = o[nt][md][0];
+              po[(size_t)hd0 * kD + dd + 8] = o[nt][md][2];
+            }
+            if (hd0 + 1 < G) {
+              po[(size_t)(hd0 + 1) * kD + dd] = o[nt][md][1];
+              po[(size_t)(hd0 + 1) * kD + dd + 8] = o[nt][md][3];
+            }
+          }
+          if (gq == 0) {
+            if (hd0 < G) *reinterpret_cast<float2*>(pm + 2 * hd0) = make_float2(mh[nt][0], lh[nt][0]);
+            if (hd0 + 1 < G) *reinterpret_cast<float2*>(pm + 2 * (hd0 + 1)) = make_float2(mh[nt][1], lh[nt][1]);
+          }
+        }
+        __syncwarp();  // (the merger's fence publishes the partial before counting it)
+        if (lane == 0) {
+          const int ms = mk % kMail;
+          if (mk >= kMail) mbar_wait(bar_mempty + 8 * ms, ((mk / kMail) - 1) & 1, p.err);
+          int* mail = reinterpret_cast<int*>(smem + lay.mail_off + ms * 16);
+          mail[0] = d.first_slot;
+          mail[1] = d.n;
+          mail[2] = b;
+          mail[3] = kh;
+          mbar_arrive(bar_mfull + 8 * ms);
+        }
+        ++mk;
+      }
+    }
+  }
+  // tell the merger that no more partials come
+  if (warp == 0 && lane == 0) {
+    const int ms = mk % kMail;
+    if (mk >= kMail) mbar_wait(bar_mempty + 8 * ms, ((mk / kMail) - 1) & 1, p.err);
+    int* mail = reinterpret_cast<int*>(smem + lay.mail_off + ms * 16);
+    mail[0] = -1;
+    mbar_arrive(bar_mfull + 8 * ms);
+  }
+}
+
+template <typename T>
+cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, uint8_t* ws, uint32_t epoch) {
+  const CUtensorMapDataType dt =
+      a.dtype == GQA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap kmap, vmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)a.B * a.Hkv * a.M};
+  const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kTile};
+  if (!encode_tensor_map(&kmap, dt, 2, a.kbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map(&vmap, dt, 2, a.vbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+
+  const int G = a.H / a.Hkv;
+  DynParams p{};
+  p.q = a.q;
+  p.knew = a.k;
+  p.vnew = a.v;
+  p.kbuf = a.kbuf;
+  p.vbuf = a.vbuf;
+  p.seqlens = a.seqlens;
+  p.cos = a.cos;
+  p.sin = a.sin;
+  p.bias = a.bias;
+  p.out = a.out;
+  p.part_o = reinterpret_cast<float*>(ws + plan.part_o_off);
+  p.part_ml = reinterpret_cast<float*>(ws + plan.part_ml_off);
+  p.ticket = reinterpret_cast<unsigned long long*>(ws + plan.sched_off);
+  p.arrivals = p.ticket + 1;
+  p.err = a.err;
+  p.B = a.B;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = G;
+  p.M = a.M;
+  p.total = a.total;
+  p.window = a.window;
+  p.P = plan.ctas;
+  p.interleaved = a.interleaved;
+  p.bias_b = a.bias_b;
+  p.bias_h = a.bias_h;
+  p.chunks_per_cta = kDecodeChunksPerCta;
+  p.epoch = epoch;
+  p.scale_log2 = a.scale * kLog2e;
+  const int smem = layout_for(G).total;
+  auto kern = G <= 8 ? decode_dyn_kernel<T, 1> : decode_dyn_kernel<T, 2>;
+  static int attr_set[64][2] = {};  // dynamic shared memory set so far, per device and variant
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int vi = G <= 8 ? 0 : 1;
+  if (dev < 0 || dev >= 64 || attr_set[dev][vi] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev][vi] = smem;
+  }
+  // programmatic dependent launch: the prologue may overlap the previous
+  // kernel's tail; the kernel waits for it before reading any input
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kmap, vmap, p);
+}
+
+}  // namespace
+
+int decode_dyn_ctas_per_sm(int G, int smem_per_sm) {
+  const size_t per = (size_t)layout_for(G).total + kSmReservedPerCta;
+  const int n = (int)((smem_per_sm > 0 ? (size_t)smem_per_sm : kSmPerSM) / per);
+  return n < 1 ? 1 : (n > 2 ? 2 : n);
+}
+
+cudaError_t launch_decode_dyn(const ForwardArgs& a, const Plan& plan, uint8_t* workspace, uint32_t epoch) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, plan, workspace, epoch)
+                                   : launch_t<__half>(a, plan, workspace, epoch);
+}
+
+}  // namespace gqa

@@ -60,6 +60,22 @@ void* scratch_address() {
 
 bool misaligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
+// Scratch of the static-partition decode kernels: two partials (o, then
+// (max, sum)) per persistent CTA, whatever the lengths.
+Plan split_plan(int B, int H, int Hkv, int D, int nsm) {
+  (void)B;
+  Plan pl{};
+  const int G = H / Hkv;
+  pl.path = Path::kDecode;
+  pl.ctas = nsm * decode_ctas_per_sm(G, device_smem_per_sm());
+  pl.part_o_off = 0;
+  pl.part_o_bytes = (size_t)pl.ctas * 2 * G * D * sizeof(float);
+  pl.part_ml_off = (pl.part_o_bytes + 255) / 256 * 256;
+  pl.part_ml_bytes = (size_t)pl.ctas * 2 * G * 2 * sizeof(float);
+  pl.total_bytes = (pl.part_ml_off + pl.part_ml_bytes + 255) / 256 * 256;
+  return pl;
+}
+
 }  // namespace
 }  // namespace gqa
 
@@ -102,8 +118,7 @@ extern "C" gqa_status_t gqa_decode_noalloc(const gqa_dims_t* dims, const void* q
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARGUMENT;
 
   const int nsm = device_sm_count();
-  const Plan pl = make_plan(B, S, H, Hkv, D, total_sequence_length, local_window_size, cos_cache != nullptr, nsm);
-  if (pl.path != Path::kDecode) return GQA_ERR_UNSUPPORTED;
+  const Plan pl = split_plan(B, H, Hkv, D, nsm);
   if (pl.total_bytes > kStaticScratchBytes) return GQA_ERR_UNSUPPORTED;  // beyond the static scratch
 
   int* err = device_error_word();

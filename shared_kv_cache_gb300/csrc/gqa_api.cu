@@ -56,6 +56,17 @@ int sm_count() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// A fresh tag for the decode counters in the workspace, per call (never 0,
+// the value the kernel leaves behind, nor all ones).
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> counter{0};
+  uint32_t e;
+  do {
+    e = counter.fetch_add(1, std::memory_order_relaxed) + 1u;
+  } while (e == 0u || e == 0xFFFFFFFFu);
+  return e;
+}
+
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 // Checks the dims alone.
@@ -92,20 +103,28 @@ int smem_per_sm() {
 // Accessors for other translation units of the library.
 int* device_error_word() { return error_word_ptr(); }
 int device_sm_count() { return sm_count(); }
+int device_smem_per_sm() { return smem_per_sm(); }
 
 Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms) {
   Plan pl{};
   const int G = H / Hkv;
   if (S == 1 && D == 128 && G <= kDecodeMaxGroup) {
-    // Persistent split-KV decode: P CTAs, each leaving at most two partials.
+    // Persistent split-KV decode with dynamic chunks: P CTAs; the items cut
+    // into several chunks hold fewer than 2 * kDecodeChunksPerCta * P partial
+    // slots in all (a chunk size C >= T / (kDecodeChunksPerCta * P) tiles,
+    // and an item of n >= 2 chunks has more than C tiles, so n < 2 tiles / C).
     pl.path = Path::kDecode;
-    pl.ctas = num_sms * decode_ctas_per_sm(G, smem_per_sm());
+    pl.ctas = num_sms * decode_dyn_ctas_per_sm(G, smem_per_sm());
+    pl.slots = 2 * kDecodeChunksPerCta * pl.ctas;
     size_t off = 0;
+    pl.sched_off = off;
+    pl.sched_bytes = (size_t)(1 + pl.slots) * sizeof(unsigned long long);
+    off = align_up(off + pl.sched_bytes, 256);
     pl.part_o_off = off;
-    pl.part_o_bytes = (size_t)pl.ctas * 2 * G * D * sizeof(float);
+    pl.part_o_bytes = (size_t)pl.slots * G * D * sizeof(float);
     off = align_up(off + pl.part_o_bytes, 256);
     pl.part_ml_off = off;
-    pl.part_ml_bytes = (size_t)pl.ctas * 2 * G * 2 * sizeof(float);
+    pl.part_ml_bytes = (size_t)pl.slots * G * 2 * sizeof(float);
     off = align_up(off + pl.part_ml_bytes, 256);
     pl.total_bytes = off;
     (void)total;
@@ -235,8 +254,7 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
   cudaError_t e = cudaSuccess;
   switch (pl.path) {
     case Path::kDecode:
-      e = launch_decode(a, pl, reinterpret_cast<float*>(ws + pl.part_o_off),
-                        reinterpret_cast<float*>(ws + pl.part_ml_off));
+      e = launch_decode_dyn(a, pl, ws, next_epoch());
       break;
     case Path::kPrefillTC:
     case Path::kGeneric: {

@@ -42,22 +42,32 @@ struct Plan {
   Path path;
   int ctas = 0;    // decode: persistent grid size P
   size_t q_rot_off = 0, q_rot_bytes = 0;    // rotated queries, T [B, S, H, D]
-  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [P, 2, G, D]
-  size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [P, 2, G, 2]
+  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [slots, G, D]
+  size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [slots, G, 2]
+  size_t sched_off = 0, sched_bytes = 0;      // decode chunk ticket + per-item arrival counters, u64 [1 + slots]
+  int slots = 0;                              // decode partial slots
   size_t total_bytes = 0;
 };
 
 Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms);
 
-// The current device's error word (device address) and SM count.
+// The current device's error word (device address), SM count and shared
+// memory per SM.
 int* device_error_word();
 int device_sm_count();
+int device_smem_per_sm();
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot);
 cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src);
+// Split-KV decode with a static partition and a separate combine kernel
+// (partials f32 [P, 2, G, D] and [P, 2, G, 2]; used by gqa_decode_noalloc).
 cudaError_t launch_decode(const ForwardArgs& a, const Plan& plan, float* part_o, float* part_ml);
 int decode_ctas_per_sm(int group, int smem_per_sm);  // resident decode CTAs per SM (1 or 2)
+// Split-KV decode with dynamic chunk scheduling and the combine inside the
+// kernel (workspace laid out by make_plan; `epoch` is unique per call).
+cudaError_t launch_decode_dyn(const ForwardArgs& a, const Plan& plan, uint8_t* workspace, uint32_t epoch);
+int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
 cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
@@ -68,5 +78,9 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ra
 // Decode kernel geometry shared by the plan and the launcher.
 constexpr int kDecodeTile = 64;     // keys per pipeline stage
 constexpr int kDecodeMaxGroup = 16;  // query heads per KV head the decode kernel supports
+#ifndef GQA_DECODE_CHUNKS_PER_CTA
+#define GQA_DECODE_CHUNKS_PER_CTA 2
+#endif
+constexpr int kDecodeChunksPerCta = GQA_DECODE_CHUNKS_PER_CTA;  // dynamic decode: chunks per persistent CTA (on average)
 
 }  // namespace gqa

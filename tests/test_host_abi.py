@@ -114,11 +114,12 @@ def test_workspace_checks(lib):
 
 
 def test_workspace_plan_decode(lib):
-    # decode at D = 128: at most two fp32 partials (G x (D + 2) floats) per
-    # persistent CTA, whatever the lengths
+    # decode at D = 128: 2 * 2 partial slots per persistent CTA (one or two
+    # CTAs per SM on 152 SMs), each G x (D + 2) fp32 values plus an 8-byte
+    # arrival counter, and the 8-byte chunk ticket -- whatever the lengths
     d = dims(seq_len=1, head_size=128, num_heads=32, kv_num_heads=8, batch=16, max_seq_len=4096)
     big = gqa.gqa_workspace_size(d, 4096, 0)
     assert big > 0 and big % 256 == 0
     assert gqa.gqa_workspace_size(d, 17, 0) == big == gqa.gqa_workspace_size(d, 4096, 100)
-    per_cta = 2 * 4 * 130 * 4
-    assert big >= 152 * per_cta and big <= 2 * 152 * per_cta + 512
+    per_slot = 4 * 130 * 4 + 8
+    assert big >= 4 * 152 * per_slot and big <= 4 * 2 * 152 * per_slot + 8 + 3 * 256
