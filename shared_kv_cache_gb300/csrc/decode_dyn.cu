@@ -429,37 +429,39 @@ __global__ void __launch_bounds__(kThreads, 2)
       ++mk;
       if (first < 0) break;  // the consumers are done
       unsigned long long* arr = p.arrivals + first;
+      if (b < 0) {
+        // a chunk of the item has started here: make sure the item's counter
+        // holds this call's epoch before this CTA counts itself in
+        if (lane == 0) epoch_install(arr, p.epoch);
+        continue;
+      }
       uint32_t cnt = 0;
       if (lane == 0) {
-        // the partial, written by consumer warp 0 before the mailbox handed
-        // it over (CTA scope), is made visible at GPU scope before the count
-        __threadfence();
-        epoch_install(arr, p.epoch);
-        cnt = epoch_take(arr, p.epoch, p.err);
+        // release: the partial, written by consumer warp 0 before the mailbox
+        // handed it over, is visible at GPU scope before the count; acquire:
+        // the last chunk sees the other chunks' partials
+        unsigned long long old;
+        asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(arr) : "memory");
+        if ((uint32_t)(old >> 32) != p.epoch) {
+          record_error(p.err, GQA_ERR_INVALID_ARGUMENT);  // the workspace changed under the call
+          cnt = 0xFFFFFFFFu;
+        } else {
+          cnt = (uint32_t)old;
+        }
       }
       cnt = __shfl_sync(0xffffffffu, cnt, 0);
       if (cnt != (uint32_t)(n - 1)) continue;
       // the item's last chunk: merge its n partials (read through L2)
-      __threadfence();
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
       T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
       const float* ml0 = p.part_ml + (size_t)first * G * 2;
       const float* po0 = p.part_o + (size_t)first * G * kD;
-      // heads four at a time; the loads of a round are independent, so a
-      // merge costs about n / 32 + n / 4 round trips to L2 per head group
+      // heads four at a time, partials four at a time with a running max: the
+      // loads of a round are independent, so a merge costs about n / 4 round
+      // trips to L2 per head group
       const int d4 = lane * 4;
       for (int g0 = 0; g0 < G; g0 += 4) {
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        for (int k = lane; k < n; k += 32) {
-#pragma unroll
-          for (int gi = 0; gi < 4; ++gi)
-            if (g0 + gi < G) mx[gi] = fmaxf(mx[gi], __ldcg(ml0 + ((size_t)k * G + g0 + gi) * 2));
-        }
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx[gi] = fmaxf(mx[gi], __shfl_xor_sync(0xffffffffu, mx[gi], o));
-          if (mx[gi] == -INFINITY) mx[gi] = 0.f;
-        }
+        float mrun[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float4 acc[4];
         float l[4];
 #pragma unroll
@@ -479,16 +481,28 @@ __global__ void __launch_bounds__(kThreads, 2)
                              : make_float2(-INFINITY, 0.f);
             }
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int gi = 0; gi < 4; ++gi) {
+            float mb = mrun[gi];
 #pragma unroll
-            for (int gi = 0; gi < 4; ++gi) {
-              const float w = fast_exp2(mlv[q][gi].x - mx[gi]);
+            for (int q = 0; q < 4; ++q) mb = fmaxf(mb, mlv[q][gi].x);
+            const float base = mb == -INFINITY ? 0.f : mb;
+            const float sc = fast_exp2(mrun[gi] - base);  // 0 while nothing has been added
+            mrun[gi] = mb;
+            l[gi] *= sc;
+            acc[gi].x *= sc;
+            acc[gi].y *= sc;
+            acc[gi].z *= sc;
+            acc[gi].w *= sc;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float w = fast_exp2(mlv[q][gi].x - base);
               l[gi] += w * mlv[q][gi].y;
               acc[gi].x += w * ov[q][gi].x;
               acc[gi].y += w * ov[q][gi].y;
               acc[gi].z += w * ov[q][gi].z;
               acc[gi].w += w * ov[q][gi].w;
             }
+          }
         }
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
@@ -519,6 +533,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const ChunkDesc d = *reinterpret_cast<const ChunkDesc*>(slot);
     if (d.u < 0) break;
     ++dk;
+    if (warp == 0 && d.slot >= 0) {
+      // tell the merger that a chunk of this item starts here
+      if (lane == 0) {
+        const int ms = mk % kMail;
+        if (mk >= kMail) mbar_wait(bar_mempty + 8 * ms, ((mk / kMail) - 1) & 1, p.err);
+        int* mail = reinterpret_cast<int*>(smem + lay.mail_off + ms * 16);
+        mail[0] = d.first_slot;
+        mail[1] = d.n;
+        mail[2] = -1;
+        mail[3] = 0;
+        mbar_arrive(bar_mfull + 8 * ms);
+      }
+      ++mk;
+    }
     const int b = d.b, kh = d.kh, klo = d.klo, L = d.L, tb = d.tb;
     const int t0 = d.t0, t1 = d.t1;
     const int past = L - 1;
