@@ -319,6 +319,8 @@ print(json.dumps({{"value": nbytes * n / dt / 1e9, "calls": n, "seconds": dt, "s
 # kernel per launch, from the ncu captures summarised in profiles/; a kernel
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
+    "decode_b16": 105395456 + 2935040,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
+    "prefill_2k": 109501952 + 30063360,    # prefill_kernel, profiles/prefill_kernel_prefill_2k.md
 }
 
 
