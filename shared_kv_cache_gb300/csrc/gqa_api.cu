@@ -132,9 +132,22 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
     return pl;
   }
   pl.path = (S > 1 && D == 128) ? Path::kPrefillTC : Path::kGeneric;
-  // the tensor-core prefill rotates its query tiles itself; the generic
-  // kernel reads queries rotated by the append kernel
-  if (rotary && pl.path == Path::kGeneric) {
+  if (pl.path == Path::kPrefillTC) {
+    // the tensor-core prefill rotates its query tiles itself; small grids
+    // split the key ranges and need room for the partials
+    pl.splits = prefill_splits(B, S, H, Hkv, total, num_sms);
+    if (pl.splits > 1) {
+      const size_t rows = prefill_split_rows(B, S, H, Hkv, pl.splits);
+      pl.part_o_off = 0;
+      pl.part_o_bytes = rows * D * sizeof(float);
+      pl.part_ml_off = align_up(pl.part_o_bytes, 256);
+      pl.part_ml_bytes = rows * 2 * sizeof(float);
+      pl.total_bytes = align_up(pl.part_ml_off + pl.part_ml_bytes, 256);
+    }
+    return pl;
+  }
+  // the generic kernel reads queries rotated by the append kernel
+  if (rotary) {
     pl.q_rot_off = 0;
     pl.q_rot_bytes = (size_t)B * S * H * D * 2;
     pl.total_bytes = align_up(pl.q_rot_bytes, 256);
@@ -261,8 +274,10 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
       void* q_rot = (cos_cache && pl.path == Path::kGeneric) ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
       e = launch_rope_append(a, q_rot);
       if (e == cudaSuccess)
-        e = pl.path == Path::kPrefillTC ? launch_prefill_tc(a, q_rot ? q_rot : query)
-                                        : launch_attn_generic(a, q_rot ? q_rot : query);
+        e = pl.path == Path::kPrefillTC
+                ? launch_prefill_tc(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
+                                    reinterpret_cast<float*>(ws + pl.part_ml_off))
+                : launch_attn_generic(a, q_rot ? q_rot : query);
       break;
     }
   }

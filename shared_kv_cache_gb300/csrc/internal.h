@@ -42,10 +42,11 @@ struct Plan {
   Path path;
   int ctas = 0;    // decode: persistent grid size P
   size_t q_rot_off = 0, q_rot_bytes = 0;    // rotated queries, T [B, S, H, D]
-  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [slots, G, D]
+  size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [slots, G, D]; prefill splits f32 [rows, D]
   size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [slots, G, 2]
   size_t sched_off = 0, sched_bytes = 0;      // decode chunk ticket + per-item arrival counters, u64 [1 + slots]
   int slots = 0;                              // decode partial slots
+  int splits = 1;                             // prefill: key-range splits per query tile
   size_t total_bytes = 0;
 };
 
@@ -68,7 +69,12 @@ int decode_ctas_per_sm(int group, int smem_per_sm);  // resident decode CTAs per
 // kernel (workspace laid out by make_plan; `epoch` is unique per call).
 cudaError_t launch_decode_dyn(const ForwardArgs& a, const Plan& plan, uint8_t* workspace, uint32_t epoch);
 int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
-cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src);
+// Tensor-core prefill; with n_split > 1 the key range of each query tile is
+// split and the partials (part_o: f32 [rows, D], part_ml: f32 [rows, 2], rows
+// from prefill_split_rows) are merged by a second kernel.
+cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml);
+int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms);
+size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,

@@ -78,7 +78,10 @@ struct PrefillParams {
   const void* cos;   // [rows, D/2] or nullptr: the query tiles are rotated here
   const void* sin;
   void* out;  // [B, S, H*D]
+  float* part_o;   // key-range splits: unnormalised O, [item][split][2][kBM][D]
+  float* part_ml;  // (reference max, sum) per row, [item][split][2][kBM][2]
   int B, S, H, Hkv, G, M, total, window, bias_b, bias_h, n_qt, n_pairs, interleaved;
+  int n_split;     // key-range splits per work item (1: none)
   float scale_log2;
 };
 
@@ -116,10 +119,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // work item: heaviest query tiles first
-  const int per_qt = p.B * p.Hkv * p.n_pairs;
+  pdl_launch_dependents();  // the split combine may be scheduled early
+
+  // work item: heaviest query tiles first; the split index is innermost
+  const int per_qt = p.B * p.Hkv * p.n_pairs * p.n_split;
   const int qt = p.n_qt - 1 - (int)(blockIdx.x / per_qt);
-  const int rem = (int)(blockIdx.x % per_qt);
+  const int rem_s = (int)(blockIdx.x % per_qt);
+  const int sp = rem_s % p.n_split;
+  const int rem = rem_s / p.n_split;
+  const int item = qt * (p.B * p.Hkv * p.n_pairs) + rem;
   const int b = rem / (p.Hkv * p.n_pairs);
   const int kh = (rem / p.n_pairs) % p.Hkv;
   const int pr = rem % p.n_pairs;
@@ -132,7 +140,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = past + p.S;
   const int kstart = p.window > 0 ? max(0, past + i0 - p.window + 1) : 0;
   const int kend = past + i1;  // one past the last key any row of the tile sees
-  const int n_kv = (kend - kstart + kBN - 1) / kBN;
+  // this CTA's share of the tile's keys: tiles [t_lo, t_lo + n_kv) of n_all
+  const int n_all = (kend - kstart + kBN - 1) / kBN;
+  const int ts = (n_all + p.n_split - 1) / p.n_split;
+  const int t_lo = sp * ts;
+  if (t_lo >= n_all) return;
+  const int n_kv = min(ts, n_all - t_lo);
+  const bool split = ts < n_all;  // partial results, merged by the combine kernel
+  const int kbase = kstart + t_lo * kBN;
   // bf16 tiles whose first row sees few keys also carry P's rounding residue
   // (P = hi + lo, both bf16; lo in the upper 64 columns of the S region) so
   // that P.V keeps fp32-level accuracy where a few keys dominate the output
@@ -182,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int zkv = b * p.Hkv + kh;
       int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int y = kstart + j * kBN;
+        const int y = kbase + j * kBN;
         const int ks = j % kKSt, vs = j % kVSt;
         if (j >= kKSt && !mbar_wait(k_empty + 8 * ks, ((j / kKSt) - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(k_full + 8 * ks, kTileBytes);
@@ -364,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float bias_unit = kLog2e / p.scale_log2;  // bias in raw score units (scale > 0)
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int k0 = kstart + j * kBN;
+      const int k0 = kbase + j * kBN;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * t, j & 1, p.err))) { ok = false; break; }
       tc::fence_after();
       const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
@@ -553,12 +568,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after();
       const float inv = 1.f / l_run;
       T* orow = static_cast<T*>(p.out) + ((size_t)(b * p.S + i) * p.H + h) * kD;
+      const size_t prow = (((size_t)item * p.n_split + sp) * 2 + t) * kBM + row;
+      if (split && i < p.S)
+        *reinterpret_cast<float2*>(p.part_ml + prow * 2) = make_float2(m_ref, l_run);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tc::ld32(tO + c * 32, r);
         tc::wait_ld();
-        if (i < p.S) {
+        if (split && i < p.S) {
+          // unnormalised O of this key range, relative to m_ref
+          float4* po = reinterpret_cast<float4*>(p.part_o + prow * kD + c * 32);
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            po[e / 4] = make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
+                                    __uint_as_float(r[e + 3]));
+        } else if (i < p.S) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 v;
@@ -580,8 +605,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merges the key-range splits of the work items that were split: per output
+// row (b, i, h), with partials (O_s, m_s, l_s) of the splits s that had keys,
+//   m* = max m_s,  o = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s.
+// One warp per row, four dimensions per lane; rows of unsplit items were
+// written by the attention kernel and are skipped.  The lengths are read
+// before waiting for the attention kernel (they are inputs).
 template <typename T>
-cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
+__global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParams p) {
+  using E = Elem<T>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 4 + warp;
+  const bool valid = r < (long long)p.B * p.S * p.H;
+  const int h = valid ? (int)(r % p.H) : 0;
+  const int i = valid ? (int)((r / p.H) % p.S) : 0;
+  const int b = valid ? (int)(r / ((long long)p.H * p.S)) : 0;
+  const int past = valid ? p.seqlens[b] : 0;
+  pdl_wait_primary();
+  if (!valid || sequence_error(past, p.S, p.M, p.total)) return;
+  const int qt = i / kBM, i0 = qt * kBM, i1 = min(i0 + kBM, p.S);
+  const int kstart = p.window > 0 ? max(0, past + i0 - p.window + 1) : 0;
+  const int n_all = (past + i1 - kstart + kBN - 1) / kBN;
+  const int ts = (n_all + p.n_split - 1) / p.n_split;
+  if (ts >= n_all) return;  // one key range: written directly
+  const int n_eff = (n_all + ts - 1) / ts;
+  const int kh = h / p.G, gi = h - kh * p.G, pr = gi >> 1, t = gi & 1;
+  const int item = qt * (p.B * p.Hkv * p.n_pairs) + (b * p.Hkv + kh) * p.n_pairs + pr;
+  const int row = i - i0;
+  auto prow = [&](int s) { return (((size_t)item * p.n_split + s) * 2 + t) * kBM + row; };
+  float ms = -INFINITY;
+  for (int s = 0; s < n_eff; ++s) ms = fmaxf(ms, p.part_ml[prow(s) * 2]);
+  const float base = ms == -INFINITY ? 0.f : ms;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  const int d4 = lane * 4;
+  for (int s = 0; s < n_eff; ++s) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + prow(s) * 2);
+    const float4 o = *reinterpret_cast<const float4*>(p.part_o + prow(s) * kD + d4);
+    const float w = fast_exp2(ml.x - base);
+    l += w * ml.y;
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
+  const float inv = 1.f / l;
+  uint2 packed;
+  packed.x = E::pack2(acc.x * inv, acc.y * inv);
+  packed.y = E::pack2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + ((size_t)(b * p.S + i) * p.H + h) * kD + d4) = packed;
+}
+
+template <typename T>
+cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml) {
   const CUtensorMapDataType dt =
       a.dtype == GQA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap qmap, kmap, vmap;
@@ -603,9 +679,30 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
   const int n_qt = (a.S + kBM - 1) / kBM;
   const int G = a.H / a.Hkv;
   const int n_pairs = (G + 1) / 2;
-  PrefillParams p{a.err,    a.seqlens, a.bias,   a.cos,  a.sin,    a.out,  a.B,          a.S,
-                  a.H,      a.Hkv,     G,        a.M,    a.total,  a.window, a.bias_b,   a.bias_h,
-                  n_qt,     n_pairs,   a.interleaved, a.scale * kLog2e};
+  PrefillParams p{};
+  p.err = a.err;
+  p.seqlens = a.seqlens;
+  p.bias = a.bias;
+  p.cos = a.cos;
+  p.sin = a.sin;
+  p.out = a.out;
+  p.part_o = part_o;
+  p.part_ml = part_ml;
+  p.B = a.B;
+  p.S = a.S;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.G = G;
+  p.M = a.M;
+  p.total = a.total;
+  p.window = a.window;
+  p.bias_b = a.bias_b;
+  p.bias_h = a.bias_h;
+  p.n_qt = n_qt;
+  p.n_pairs = n_pairs;
+  p.interleaved = a.interleaved;
+  p.n_split = n_split;
+  p.scale_log2 = a.scale * kLog2e;
   auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
   static bool attr_set[64][2] = {};  // per device and instantiation
   int dev = 0;
@@ -616,15 +713,47 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev][vi] = true;
   }
-  const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt;
+  const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
   kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || n_split == 1) return e;
+  // the split combine, overlapping the attention kernel's tail
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(((long long)a.B * a.S * a.H + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_combine_kernel<T>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src) {
-  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src) : launch_t<__half>(a, q_src);
+int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms) {
+  // A grid of fewer than two CTAs per SM cuts the key range of each query
+  // tile into up to 3 * SMs / CTAs pieces (no more than it has key tiles),
+  // so that the long key ranges do not set the time.
+  const int n_qt = (S + kBM - 1) / kBM;
+  const int G = H / Hkv;
+  const long long base = (long long)B * Hkv * ((G + 1) / 2) * n_qt;
+  if (base >= 2ll * num_sms) return 1;
+  const int max_tiles = (total + kBN - 1) / kBN + 1;
+  const int want = (int)((3ll * num_sms + base - 1) / base);
+  return want < 1 ? 1 : (want > max_tiles ? max_tiles : want);
+}
+size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split) {
+  // rows of partial results: items x splits x 2 query tiles x kBM rows
+  const int n_qt = (S + kBM - 1) / kBM;
+  const int G = H / Hkv;
+  return (size_t)B * Hkv * ((G + 1) / 2) * n_qt * n_split * 2 * kBM;
+}
+
+cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src, n_split, part_o, part_ml)
+                                   : launch_t<__half>(a, q_src, n_split, part_o, part_ml);
 }
 
 }  // namespace gqa
