@@ -217,6 +217,55 @@ __device__ Partition make_partition(const DynParams& p, const int* sl, int lane)
   return Partition{C, U * p.Hkv};
 }
 
+// Chunk u within one block of 32 sequences b0 + lane, given each lane's tile
+// count, key range and the block's inclusive scans of chunks (incl) and
+// partial slots (sincl); cbase / sbase count those of earlier blocks.
+__device__ __forceinline__ ChunkDesc chunk_in_block(const DynParams& p, const Partition& pt, int u, int b0, int tb,
+                                                    int lo, int L, int nb, int ch, int sl_n, int incl, int sincl,
+                                                    int cbase, int sbase) {
+  const unsigned m = __ballot_sync(0xffffffffu, cbase + incl > u);
+  const int l = __ffs(m) - 1;
+  ChunkDesc d;
+  d.b = b0 + l;
+  const int c0 = cbase + __shfl_sync(0xffffffffu, incl - ch, l);
+  const int s0 = sbase + __shfl_sync(0xffffffffu, sincl - sl_n, l);
+  d.tb = __shfl_sync(0xffffffffu, tb, l);
+  d.klo = __shfl_sync(0xffffffffu, lo, l);
+  d.L = __shfl_sync(0xffffffffu, L, l);
+  d.n = __shfl_sync(0xffffffffu, nb, l);
+  const int r = u - c0;
+  d.kh = r / d.n;
+  const int k = r - d.kh * d.n;
+  d.t0 = k * pt.C;
+  d.t1 = min(d.t0 + pt.C, d.tb);
+  d.u = u;
+  d.first_slot = d.n > 1 ? s0 + d.kh * d.n : -1;
+  d.slot = d.n > 1 ? d.first_slot + k : -1;
+  return d;
+}
+
+// Batches of at most 32 sequences: the partition and chunk u (u < 0: none)
+// in one warp pass.
+__device__ ChunkDesc partition_and_locate_small(const DynParams& p, const int* sl, int u, int lane, Partition& pt) {
+  int lo = 0, L = 0;
+  const int tb = lane < p.B ? seq_tiles(p, sl[lane], lo, L) : 0;
+  const int T = warp_sum(tb) * p.Hkv;
+  const int target = p.chunks_per_cta * p.P;
+  pt.C = max(2, (T + target - 1) / target);
+  const int nb = (tb + pt.C - 1) / pt.C;
+  const int ch = nb * p.Hkv;
+  const int sl_n = nb > 1 ? ch : 0;
+  const int incl = warp_incl_scan(ch, lane);
+  const int sincl = warp_incl_scan(sl_n, lane);
+  pt.U = __shfl_sync(0xffffffffu, incl, 31);
+  if (u < 0 || u >= pt.U) {
+    ChunkDesc d{};
+    d.u = -1;
+    return d;
+  }
+  return chunk_in_block(p, pt, u, 0, tb, lo, L, nb, ch, sl_n, incl, sincl, 0, 0);
+}
+
 // Warp-cooperative: the item and tile range of chunk u (< U).
 __device__ ChunkDesc locate_chunk(const DynParams& p, const int* sl, const Partition& pt, int u, int lane) {
   int cbase = 0, sbase = 0;  // chunks and partial slots of the sequences before b0
@@ -230,27 +279,8 @@ __device__ ChunkDesc locate_chunk(const DynParams& p, const int* sl, const Parti
     const int incl = warp_incl_scan(ch, lane);
     const int sincl = warp_incl_scan(sl_n, lane);
     const int chunk_total = __shfl_sync(0xffffffffu, incl, 31);
-    if (u < cbase + chunk_total) {
-      const unsigned m = __ballot_sync(0xffffffffu, cbase + incl > u);
-      const int l = __ffs(m) - 1;
-      ChunkDesc d;
-      d.b = b0 + l;
-      const int c0 = cbase + __shfl_sync(0xffffffffu, incl - ch, l);
-      const int s0 = sbase + __shfl_sync(0xffffffffu, sincl - sl_n, l);
-      d.tb = __shfl_sync(0xffffffffu, tb, l);
-      d.klo = __shfl_sync(0xffffffffu, lo, l);
-      d.L = __shfl_sync(0xffffffffu, L, l);
-      d.n = __shfl_sync(0xffffffffu, nb, l);
-      const int r = u - c0;
-      d.kh = r / d.n;
-      const int k = r - d.kh * d.n;
-      d.t0 = k * pt.C;
-      d.t1 = min(d.t0 + pt.C, d.tb);
-      d.u = u;
-      d.first_slot = d.n > 1 ? s0 + d.kh * d.n : -1;
-      d.slot = d.n > 1 ? d.first_slot + k : -1;
-      return d;
-    }
+    if (u < cbase + chunk_total)
+      return chunk_in_block(p, pt, u, b0, tb, lo, L, nb, ch, sl_n, incl, sincl, cbase, sbase);
     cbase += chunk_total;
     sbase += __shfl_sync(0xffffffffu, sincl, 31);
   }
@@ -318,16 +348,47 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int e = sequence_error(sl[i], 1, p.M, p.total);
         if (e) record_error(p.err, e);
       }
-    const Partition pt = make_partition(p, sl, lane);
+    Partition pt;
+    ChunkDesc first{};
+    if (p.B <= 32) {
+      first = partition_and_locate_small(p, sl, c, lane, pt);
+    } else {
+      pt = make_partition(p, sl, lane);
+      first.u = -1;
+      if (c < pt.U) first = locate_chunk(p, sl, pt, c, lane);
+    }
     const bool rot = p.cos != nullptr;
-    int u = c < pt.U ? c : -1;
+    int u = first.u;
     int gt = 0;  // tiles issued by this CTA
-    int dk = 0;  // descriptors issued
     bool ok = true;
+    // (lane 0) K/V tiles [ta, tb_) of chunk d into the ring
+    auto issue_tiles = [&](const ChunkDesc& d, int ta, int tb_) {
+      const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo;
+      for (int t = ta; t < tb_ && ok; ++t, ++gt) {
+        const int st = gt % kStages;
+        const int round = gt / kStages;
+        if (round > 0 && !mbar_wait(bar_empty + 8 * st, (round - 1) & 1, p.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bar_full + 8 * st;
+        const uint32_t kd = sbase + st * kStageBytes;
+        const uint32_t vd = kd + kTileBytes;
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        const int y = row0 + t * kTile;
+        tma_load_2d(kd, &kmap, 0, y, fb);
+        tma_load_2d(kd + kBoxBytes, &kmap, 64, y, fb);
+        tma_load_2d(vd, &vmap, 0, y, fb);
+        tma_load_2d(vd + kBoxBytes, &vmap, 64, y, fb);
+      }
+    };
+    int dk = 0;  // descriptors issued
     bool first_take = true;
     while (true) {
       ChunkDesc d;
-      if (u >= 0) {
+      if (dk == 0) {
+        d = first;
+      } else if (u >= 0) {
         d = locate_chunk(p, sl, pt, u, lane);
       } else {
         d = ChunkDesc{};
@@ -364,26 +425,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       ++dk;
       if (d.u < 0 || !ok) break;
-      if (lane == 0) {
-        const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo;
-        for (int t = d.t0; t < d.t1; ++t, ++gt) {
-          const int st = gt % kStages;
-          const int round = gt / kStages;
-          if (round > 0 && !mbar_wait(bar_empty + 8 * st, (round - 1) & 1, p.err)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = bar_full + 8 * st;
-          const uint32_t kd = sbase + st * kStageBytes;
-          const uint32_t vd = kd + kTileBytes;
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          const int y = row0 + t * kTile;
-          tma_load_2d(kd, &kmap, 0, y, fb);
-          tma_load_2d(kd + kBoxBytes, &kmap, 64, y, fb);
-          tma_load_2d(vd, &vmap, 0, y, fb);
-          tma_load_2d(vd + kBoxBytes, &vmap, 64, y, fb);
-        }
-      }
+      // (after the descriptor: its small staging copies must not queue
+      // behind the tiles)
+      if (lane == 0) issue_tiles(d, d.t0, d.t1);
       gt = __shfl_sync(0xffffffffu, gt, 0);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       // the next chunk's ticket (its latency hides behind the tiles queued in
