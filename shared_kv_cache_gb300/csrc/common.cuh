@@ -226,27 +226,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x on the FMA pipe, for spreading exponentials over two execution units:
-// x = n + f with n = round(x) (adding and subtracting 1.5 * 2^23 rounds to the
-// nearest integer), 2^f for f in [-1/2, 1/2] by a degree-4 polynomial
-// (least-squares fit at 200 Chebyshev nodes, reweighted toward the minimax
-// relative error: 2.7e-6 in fp32 Horner evaluation), and 2^n added to the
-// exponent field.  Valid for x <= 127; x below -125 (including -inf) gives 0.
-__device__ __forceinline__ float exp2_poly(float x) {
-  const float xc = fmaxf(x, -125.f);
-  const float t = xc + 12582912.f;
-  const float n = t - 12582912.f;
-  const float fr = xc - n;
-  float q = 0.009570096619427204f;
-  q = fmaf(q, fr, 0.05591785907745361f);
-  q = fmaf(q, fr, 0.240247443318367f);
-  q = fmaf(q, fr, 0.6931217908859253f);
-  q = fmaf(q, fr, 0.9999992847442627f);
-  const int ni = __float_as_int(t) - 0x4B400000;  // n as an integer
-  const float y = __int_as_float(__float_as_int(q) + (ni << 23));
-  return x >= -125.f ? y : 0.f;
-}
-
 // Transpose of an 8x8 matrix of 16-bit values held one 32-bit register per
 // thread in the mma fragment layout.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {

@@ -65,10 +65,6 @@ constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1;
 constexpr int kSlotOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kSlotOff + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
-#ifndef GQA_PREFILL_POLY_EVERY
-#define GQA_PREFILL_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = GQA_PREFILL_POLY_EVERY;  // 0: every exponential on the special-function unit
 constexpr float kRescaleThresh = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
 struct PrefillParams {
@@ -480,8 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= f_resc;
       }
       // P = 2^(s - m) as 16-bit pairs over the first 64 columns of S (every
-      // score is already in registers); one pair in kPolyEvery is
-      // exponentiated on the FMA pipe to relieve the special-function unit
+      // score is already in registers)
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       const float sc = p.scale_log2;
       float rs[4] = {0.f, 0.f, 0.f, 0.f};
@@ -495,9 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 16; ++e) {
             const float x0 = fmaf(__uint_as_float(sv[c][2 * e]), sc, -mu);
             const float x1 = fmaf(__uint_as_float(sv[c][2 * e + 1]), sc, -mu);
-            const bool poly = kPolyEvery > 0 && (e % kPolyEvery) == kPolyEvery - 1;
-            const float a = poly ? exp2_poly(x0) : fast_exp2(x0);
-            const float bb = poly ? exp2_poly(x1) : fast_exp2(x1);
+            const float a = fast_exp2(x0);
+            const float bb = fast_exp2(x1);
             rs[e & 3] += a + bb;
             pk[e] = E::pack2(a, bb);
             if (kSplit) {  // keep P in fp32 for its rounding residue below
