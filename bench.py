@@ -119,6 +119,7 @@ class ClockSampler:
 
     def summary(self, t0, t1):
         rows = [r for (t, r) in self.samples if t0 <= t <= t1 and len(r) >= 9]
+        in_window = bool(rows)
         if not rows:
             rows = [r for (_, r) in self.samples if len(r) >= 9]
         if not rows:
@@ -136,7 +137,7 @@ class ClockSampler:
                 if v.strip().lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
-                "reasons": sorted(reasons), "samples": len(rows),
+                "reasons": sorted(reasons), "samples": len(rows), "in_window": in_window,
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
@@ -364,7 +365,6 @@ def run_ours(args):
             torch.cuda.synchronize()
     torch.cuda.synchronize()
     ms, t0, t1 = time_steps(prob, args.steps, max(args.warmup, 3), stream, ws, device)
-    sampler.stop()
     clocks = sampler.summary(tb, t1)
     rate = work / (ms * 1e-3)
     value = rate * ws
@@ -396,18 +396,28 @@ def run_ours(args):
             kvo = 2 * wo.batch * wo.kv_num_heads * wo.max_seq_len * wo.head_size * 2
             p2 = Problem(other, device, sets=4 if kvo < (1 << 30) else 1)
             steps = 20 if not p2.decode else 50
-            m, _, _ = time_steps(p2, steps, 3, stream, ws, device)
+            # ~0.5 s of load first, so that the clock samples cover this workload
+            tb2 = time.time()
+            k = 0
+            while time.time() - tb2 < 0.5:
+                p2.step(k, stream)
+                k += 1
+                if k % 50 == 0:
+                    torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            m, _, t2 = time_steps(p2, steps, 3, stream, ws, device)
             mt, un, wk = metric_of(p2)
             v = wk / (m * 1e-3)
             peak = pk["hbm_gbs"] if p2.decode else pk["bf16_tflops"]
             entry = {"workload": other, "metric": mt, "value": v, "unit": un, "ms_per_step": m,
-                     "frac": v / peak, "peak": peak}
+                     "frac": v / peak, "peak": peak, "clocks": sampler.summary(tb2, t2)}
             if not p2.decode:
                 entry["kv_gbs"] = p2.bytes / (m * 1e-3) / 1e9
             also.append(entry)
             del p2
             torch.cuda.empty_cache()
 
+    sampler.stop()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu and not args.quick and prob.decode:
         cpu = cpu_baseline(name)
