@@ -13,11 +13,14 @@ _DT = {torch.float16: B.GQA_DTYPE_FP16, torch.bfloat16: B.GQA_DTYPE_BF16}
 
 
 class Workspace:
-    """A grow-only device scratch buffer for gqa_forward."""
+    """A grow-only device scratch buffer for gqa_forward.  It also remembers
+    the dims struct and scratch size of the shapes it has served, so that a
+    decode loop pays for them once."""
 
     def __init__(self, device=None):
         self.device = device
         self.buf: Optional[torch.Tensor] = None
+        self.plans = {}
 
     def get(self, nbytes: int, device) -> Optional[torch.Tensor]:
         if nbytes == 0:
@@ -42,9 +45,20 @@ def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, n
             output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
     """One GroupQueryAttention step; k_buf/v_buf are updated in place (the
     shared past/present binding).  Returns the output tensor [B, S, H*D]."""
-    dims = dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias, rotary_interleaved)
-    nbytes = B.gqa_workspace_size(dims, total_sequence_length, local_window_size)
-    ws = (workspace or Workspace()).get(nbytes, query.device)
+    workspace = workspace or Workspace()
+    key_ = (tuple(query.shape), query.dtype, tuple(k_buf.shape), num_heads, kv_num_heads,
+            None if cos_cache is None else cos_cache.shape[0],
+            None if attention_bias is None else tuple(attention_bias.shape[:2]), rotary_interleaved,
+            int(total_sequence_length), int(local_window_size))
+    plan = workspace.plans.get(key_)
+    if plan is None:
+        dims = dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias, rotary_interleaved)
+        plan = (dims, B.gqa_workspace_size(dims, total_sequence_length, local_window_size))
+        if len(workspace.plans) > 64:
+            workspace.plans.clear()
+        workspace.plans[key_] = plan
+    dims, nbytes = plan
+    ws = workspace.get(nbytes, query.device)
     if output is None:
         output = torch.empty_like(query)
     if stream is None:

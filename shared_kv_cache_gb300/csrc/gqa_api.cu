@@ -168,11 +168,51 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ra
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
-  if (!fn) return false;
+  if (!fn || rank < 1 || rank > 5) return false;
+  // A decode loop encodes the same few maps every call: a small per-thread
+  // cache keyed by every argument (the map is a pure function of them).
+  struct Entry {
+    bool used;
+    CUtensorMapDataType type;
+    cuuint32_t rank;
+    void* base;
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t box[5];
+    CUtensorMapSwizzle swizzle;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (int e = 0; e < kEntries; ++e) {
+    const Entry& c = cache[e];
+    if (!c.used || c.type != type || c.rank != rank || c.base != base || c.swizzle != swizzle) continue;
+    bool same = true;
+    for (cuuint32_t d = 0; d < rank && same; ++d)
+      same = c.dims[d] == dims[d] && c.box[d] == box[d] && (d + 1 == rank || c.strides[d] == strides_bytes[d]);
+    if (same) {
+      *map = c.map;
+      return true;
+    }
+  }
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r = fn(map, type, rank, base, dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (r != CUDA_SUCCESS) return false;
+  Entry& c = cache[next];
+  next = (next + 1) % kEntries;
+  c.used = true;
+  c.type = type;
+  c.rank = rank;
+  c.base = base;
+  c.swizzle = swizzle;
+  for (cuuint32_t d = 0; d < rank; ++d) {
+    c.dims[d] = dims[d];
+    c.box[d] = box[d];
+    if (d + 1 < rank) c.strides[d] = strides_bytes[d];
+  }
+  c.map = *map;
+  return true;
 }
 
 }  // namespace gqa
