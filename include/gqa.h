@@ -173,6 +173,51 @@ gqa_status_t gqa_decode_noalloc(const gqa_dims_t* dims,
                                 void* output,
                                 void* stream);
 
+/*
+ * gqa_forward_host -- gqa_forward with the step's per-call inputs and its
+ * output in page-locked HOST memory, for a caller whose step data lives on
+ * the host while the shared buffer stays resident on the device.
+ *
+ *   query, key, value, seqlens_k, output
+ *                    host, page-locked (cudaHostAlloc/cudaMallocHost, or
+ *                    cudaHostRegister), same types and layouts as in
+ *                    gqa_forward; query, key, value and output 16-byte
+ *                    aligned, seqlens_k 4-byte aligned.  Any other pointer
+ *                    (pageable or device memory) returns
+ *                    GQA_ERR_INVALID_ARGUMENT before any launch.
+ *   past_key, past_value, present_key, present_value, cos_cache, sin_cache,
+ *   attention_bias   device, as in gqa_forward.
+ *   workspace        device scratch of at least gqa_workspace_size_host()
+ *                    bytes: gqa_forward's scratch plus device copies of the
+ *                    step's inputs and output.
+ *
+ * The call enqueues three stages on `stream`: a copy kernel that reads the
+ * inputs from host memory into the workspace, gqa_forward's kernels on those
+ * copies, and a copy kernel that writes the output to host memory.  The
+ * output is valid once the stream reaches that point (e.g. after
+ * cudaStreamSynchronize).  The caller must not change the host inputs, or
+ * read the host output, before then.  Error behaviour is gqa_forward's.
+ */
+gqa_status_t gqa_forward_host(const gqa_dims_t* dims,
+                              const void* query, const void* key, const void* value,
+                              const void* past_key, const void* past_value,
+                              void* present_key, void* present_value,
+                              const int32_t* seqlens_k, int32_t total_sequence_length,
+                              const void* cos_cache, const void* sin_cache,
+                              float scale, int32_t local_window_size,
+                              const void* attention_bias,
+                              void* output,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * gqa_workspace_size_host -- bytes of device scratch gqa_forward_host needs
+ * (gqa_workspace_size() rounded up to 256, plus the staged query, key,
+ * value, seqlens_k and output, each rounded up to 256).  0 for invalid dims.
+ */
+size_t gqa_workspace_size_host(const gqa_dims_t* dims, int32_t total_sequence_length,
+                               int32_t local_window_size);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ GQA_DTYPE_FP16 = 0
 GQA_DTYPE_BF16 = 1
 
 EXPORTED = ("gqa_forward", "gqa_workspace_size", "gqa_check_device_status", "gqa_status_string",
-            "gqa_decode_noalloc")
+            "gqa_decode_noalloc", "gqa_forward_host", "gqa_workspace_size_host")
 
 
 class gqa_dims_t(ctypes.Structure):
@@ -51,8 +51,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gqa_forward.restype = ctypes.c_int
     lib.gqa_forward.argtypes = [ctypes.POINTER(gqa_dims_t), vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, f32,
                                 i32, vp, vp, vp, sz, vp]
+    lib.gqa_forward_host.restype = ctypes.c_int
+    lib.gqa_forward_host.argtypes = lib.gqa_forward.argtypes
     lib.gqa_workspace_size.restype = sz
     lib.gqa_workspace_size.argtypes = [ctypes.POINTER(gqa_dims_t), i32, i32]
+    lib.gqa_workspace_size_host.restype = sz
+    lib.gqa_workspace_size_host.argtypes = [ctypes.POINTER(gqa_dims_t), i32, i32]
     lib.gqa_check_device_status.restype = ctypes.c_int
     lib.gqa_check_device_status.argtypes = [vp]
     lib.gqa_status_string.restype = ctypes.c_char_p
@@ -99,6 +103,19 @@ def gqa_forward(dims, query, key, value, past_key, past_value, present_key, pres
                            int(workspace_bytes), _stream(stream))
 
 
+def gqa_forward_host(dims, query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
+                     total_sequence_length, cos_cache, sin_cache, scale, local_window_size, attention_bias,
+                     output, workspace, workspace_bytes, stream=None) -> int:
+    """gqa_forward with query/key/value/seqlens_k/output in page-locked host
+    memory (e.g. pinned CPU tensors); the rest as in gqa_forward."""
+    lib = load_library()
+    return lib.gqa_forward_host(ctypes.byref(dims), _ptr(query), _ptr(key), _ptr(value), _ptr(past_key),
+                                _ptr(past_value), _ptr(present_key), _ptr(present_value), _ptr(seqlens_k),
+                                int(total_sequence_length), _ptr(cos_cache), _ptr(sin_cache), float(scale),
+                                int(local_window_size), _ptr(attention_bias), _ptr(output), _ptr(workspace),
+                                int(workspace_bytes), _stream(stream))
+
+
 def gqa_decode_noalloc(dims, query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
                        total_sequence_length, cos_cache, sin_cache, scale, local_window_size, attention_bias,
                        output, stream=None) -> int:
@@ -115,6 +132,11 @@ def gqa_decode_noalloc(dims, query, key, value, past_key, past_value, present_ke
 def gqa_workspace_size(dims, total_sequence_length, local_window_size=0) -> int:
     return load_library().gqa_workspace_size(ctypes.byref(dims), int(total_sequence_length),
                                              int(local_window_size))
+
+
+def gqa_workspace_size_host(dims, total_sequence_length, local_window_size=0) -> int:
+    return load_library().gqa_workspace_size_host(ctypes.byref(dims), int(total_sequence_length),
+                                                  int(local_window_size))
 
 
 def gqa_check_device_status(stream=None) -> int:

@@ -40,24 +40,31 @@ def dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache=None, attenti
     return B.make_dims(Bsz, S, num_heads, kv_num_heads, D, M, _DT[query.dtype], rotary_interleaved, rows, bb, bh)
 
 
-def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, num_heads, kv_num_heads,
-            cos_cache=None, sin_cache=None, scale=0.0, local_window_size=0, attention_bias=None,
-            output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
-    """One GroupQueryAttention step; k_buf/v_buf are updated in place (the
-    shared past/present binding).  Returns the output tensor [B, S, H*D]."""
-    workspace = workspace or Workspace()
-    key_ = (tuple(query.shape), query.dtype, tuple(k_buf.shape), num_heads, kv_num_heads,
+def _plan(workspace, host, query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias,
+          rotary_interleaved, total_sequence_length, local_window_size):
+    key_ = (host, tuple(query.shape), query.dtype, tuple(k_buf.shape), num_heads, kv_num_heads,
             None if cos_cache is None else cos_cache.shape[0],
             None if attention_bias is None else tuple(attention_bias.shape[:2]), rotary_interleaved,
             int(total_sequence_length), int(local_window_size))
     plan = workspace.plans.get(key_)
     if plan is None:
         dims = dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias, rotary_interleaved)
-        plan = (dims, B.gqa_workspace_size(dims, total_sequence_length, local_window_size))
+        size = B.gqa_workspace_size_host if host else B.gqa_workspace_size
+        plan = (dims, size(dims, total_sequence_length, local_window_size))
         if len(workspace.plans) > 64:
             workspace.plans.clear()
         workspace.plans[key_] = plan
-    dims, nbytes = plan
+    return plan
+
+
+def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, num_heads, kv_num_heads,
+            cos_cache=None, sin_cache=None, scale=0.0, local_window_size=0, attention_bias=None,
+            output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
+    """One GroupQueryAttention step; k_buf/v_buf are updated in place (the
+    shared past/present binding).  Returns the output tensor [B, S, H*D]."""
+    workspace = workspace or Workspace()
+    dims, nbytes = _plan(workspace, False, query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias,
+                         rotary_interleaved, total_sequence_length, local_window_size)
     ws = workspace.get(nbytes, query.device)
     if output is None:
         output = torch.empty_like(query)
@@ -68,4 +75,28 @@ def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, n
                        0 if ws is None else ws.numel(), stream)
     if st != B.GQA_OK:
         raise B.GqaError(st)
+    return output
+
+
+def forward_host(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, num_heads, kv_num_heads,
+                 cos_cache=None, sin_cache=None, scale=0.0, local_window_size=0, attention_bias=None,
+                 output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
+    """forward() with query/key/value/seqlens_k and the output as pinned CPU
+    tensors (gqa_forward_host); k_buf, v_buf, the caches and the bias stay on
+    the device.  The returned output is valid once `stream` has reached the
+    end of the step (synchronise it before reading)."""
+    workspace = workspace or Workspace()
+    dev = k_buf.device
+    dims, nbytes = _plan(workspace, True, query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias,
+                         rotary_interleaved, total_sequence_length, local_window_size)
+    ws = workspace.get(nbytes, dev)
+    if output is None:
+        output = torch.empty(query.shape, dtype=query.dtype, pin_memory=True)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    st = B.gqa_forward_host(dims, query, key, value, k_buf, v_buf, k_buf, v_buf, seqlens_k, total_sequence_length,
+                            cos_cache, sin_cache, scale, local_window_size, attention_bias, output, ws,
+                            0 if ws is None else ws.numel(), stream)
+    if st != B.GQA_OK:
+        raise B.GqaError(st, "gqa_forward_host")
     return output

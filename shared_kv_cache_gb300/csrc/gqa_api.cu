@@ -240,12 +240,19 @@ size_t gqa_workspace_size(const gqa_dims_t* dims, int32_t total_sequence_length,
   return pl.total_bytes;
 }
 
-gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
-                         const void* past_key, const void* past_value, void* present_key, void* present_value,
-                         const int32_t* seqlens_k, int32_t total_sequence_length, const void* cos_cache,
-                         const void* sin_cache, float scale, int32_t local_window_size,
-                         const void* attention_bias, void* output, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+}  // extern "C"
+
+namespace {
+
+// gqa_forward with optional staging copies around the step: stage_in runs
+// after every check has passed and before the step's kernels, stage_out
+// after them.
+gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
+                          const void* past_key, const void* past_value, void* present_key, void* present_value,
+                          const int32_t* seqlens_k, int32_t total_sequence_length, const void* cos_cache,
+                          const void* sin_cache, float scale, int32_t local_window_size,
+                          const void* attention_bias, void* output, void* workspace, size_t workspace_bytes,
+                          void* stream, const StageList* stage_in, const StageList* stage_out) {
   gqa_status_t st = check_dims(dims);
   if (st != GQA_OK) return st;
   const int B = dims->batch, S = dims->seq_len, H = dims->num_heads, Hkv = dims->kv_num_heads;
@@ -304,7 +311,8 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
   a.num_sms = nsm;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = stage_in ? launch_stage(*stage_in, a.stream, nsm) : cudaSuccess;
+  if (e != cudaSuccess) return GQA_ERR_CUDA;
   switch (pl.path) {
     case Path::kDecode:
       e = launch_decode_dyn(a, pl, ws, next_epoch());
@@ -321,7 +329,99 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
       break;
     }
   }
+  if (e == cudaSuccess && stage_out) e = launch_stage(*stage_out, a.stream, nsm);
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+// The device address of page-locked host memory (allocated or registered by
+// CUDA), or nullptr for any other pointer.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // not a CUDA pointer: clear the (non-sticky) error
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// gqa_forward_host's workspace: gqa_forward's scratch, then the device copies
+// of the step's inputs and output, each 256-byte aligned.
+struct HostStaging {
+  size_t q, k, v, s, o, total;
+  size_t qb, kb, sb;  // bytes of query (= output), key (= value), seqlens_k
+  size_t base;        // gqa_forward's part
+};
+HostStaging host_staging(const gqa_dims_t* d, int32_t total, int32_t window) {
+  HostStaging h{};
+  const size_t rows = (size_t)d->batch * d->seq_len;
+  h.qb = rows * d->num_heads * d->head_size * 2;
+  h.kb = rows * d->kv_num_heads * d->head_size * 2;
+  h.sb = (size_t)d->batch * 4;
+  h.base = align_up(gqa_workspace_size(d, total, window), 256);
+  h.q = h.base;
+  h.k = h.q + align_up(h.qb, 256);
+  h.v = h.k + align_up(h.kb, 256);
+  h.s = h.v + align_up(h.kb, 256);
+  h.o = h.s + align_up(h.sb, 256);
+  h.total = h.o + align_up(h.qb, 256);
+  return h;
+}
+
+}  // namespace
+
+extern "C" {
+
+gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
+                         const void* past_key, const void* past_value, void* present_key, void* present_value,
+                         const int32_t* seqlens_k, int32_t total_sequence_length, const void* cos_cache,
+                         const void* sin_cache, float scale, int32_t local_window_size,
+                         const void* attention_bias, void* output, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return forward_impl(dims, query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
+                      total_sequence_length, cos_cache, sin_cache, scale, local_window_size, attention_bias, output,
+                      workspace, workspace_bytes, stream, nullptr, nullptr);
+}
+
+size_t gqa_workspace_size_host(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size) {
+  if (check_dims(dims) != GQA_OK || total_sequence_length < dims->seq_len) return 0;
+  return host_staging(dims, total_sequence_length, local_window_size).total;
+}
+
+gqa_status_t gqa_forward_host(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
+                              const void* past_key, const void* past_value, void* present_key,
+                              void* present_value, const int32_t* seqlens_k, int32_t total_sequence_length,
+                              const void* cos_cache, const void* sin_cache, float scale,
+                              int32_t local_window_size, const void* attention_bias, void* output,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  gqa_status_t st = check_dims(dims);
+  if (st != GQA_OK) return st;
+  if (!key && !value) return GQA_ERR_UNSUPPORTED;
+  if (!query || !key || !value || !seqlens_k || !output) return GQA_ERR_INVALID_ARGUMENT;
+  if (misaligned(query) || misaligned(key) || misaligned(value) || misaligned(output) ||
+      (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
+    return GQA_ERR_INVALID_ARGUMENT;
+  if (total_sequence_length < dims->seq_len) return GQA_ERR_INVALID_ARGUMENT;
+  const HostStaging h = host_staging(dims, total_sequence_length, local_window_size);
+  if (!workspace || workspace_bytes < h.total || misaligned(workspace)) return GQA_ERR_INVALID_ARGUMENT;
+  void* dq = mapped_host(query);
+  void* dk = mapped_host(key);
+  void* dv = mapped_host(value);
+  void* ds = mapped_host(seqlens_k);
+  void* dout = mapped_host(output);
+  if (!dq || !dk || !dv || !ds || !dout) return GQA_ERR_INVALID_ARGUMENT;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  StageList in;
+  in.seg[0] = StageSeg{dq, ws + h.q, h.qb};
+  in.seg[1] = StageSeg{dk, ws + h.k, h.kb};
+  in.seg[2] = StageSeg{dv, ws + h.v, h.kb};
+  in.seg[3] = StageSeg{ds, ws + h.s, h.sb};
+  in.n = 4;
+  StageList out;
+  out.seg[0] = StageSeg{ws + h.o, dout, h.qb};
+  out.n = 1;
+  return forward_impl(dims, ws + h.q, ws + h.k, ws + h.v, past_key, past_value, present_key, present_value,
+                      reinterpret_cast<const int32_t*>(ws + h.s), total_sequence_length, cos_cache, sin_cache,
+                      scale, local_window_size, attention_bias, ws + h.o, workspace, h.base, stream, &in, &out);
 }
 
 gqa_status_t gqa_check_device_status(void* stream) {

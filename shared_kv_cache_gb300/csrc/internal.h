@@ -76,6 +76,22 @@ cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_spl
 int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms);
 size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split);
 
+// Staging copies of up to kMaxStageSegs byte ranges (each a multiple of 4
+// bytes at 4-byte aligned addresses; either side may be page-locked host
+// memory at its device address), by a kernel launched with programmatic
+// dependent launch that waits for the previous kernel before it writes.
+constexpr int kMaxStageSegs = 4;
+struct StageSeg {
+  const void* src;
+  void* dst;
+  size_t bytes;
+};
+struct StageList {
+  StageSeg seg[kMaxStageSegs];
+  int n = 0;
+};
+cudaError_t launch_stage(const StageList& l, cudaStream_t stream, int num_sms);
+
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,
                        const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,

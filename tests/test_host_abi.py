@@ -123,3 +123,34 @@ def test_workspace_plan_decode(lib):
     assert gqa.gqa_workspace_size(d, 17, 0) == big == gqa.gqa_workspace_size(d, 4096, 100)
     per_slot = 4 * 130 * 4 + 8
     assert big >= 4 * 152 * per_slot and big <= 4 * 2 * 152 * per_slot + 8 + 3 * 256
+
+
+def call_host(dims, total=64, **over):
+    a = dict(query=P["q"], key=P["k"], value=P["v"], past_key=P["kb"], past_value=P["vb"],
+             present_key=P["kb"], present_value=P["vb"], seqlens_k=P["seq"], total_sequence_length=total,
+             cos_cache=P["cos"], sin_cache=P["sin"], scale=0.0, local_window_size=0, attention_bias=None,
+             output=P["out"], workspace=P["ws"], workspace_bytes=1 << 30)
+    a.update(over)
+    return gqa.gqa_forward_host(dims, **a)
+
+
+def test_host_entry_workspace_and_checks(lib):
+    # gqa_forward's scratch rounded to 256, then query, key, value, seqlens_k
+    # and output copies, each rounded to 256 bytes
+    d = dims()  # B 2, S 4, H 8, Hkv 2, D 64, fp16
+    base = gqa.gqa_workspace_size(d, 64, 0)
+    qb, kb, sb = 2 * 4 * 8 * 64 * 2, 2 * 4 * 2 * 64 * 2, 2 * 4
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    need = gqa.gqa_workspace_size_host(d, 64, 0)
+    assert need == r(base) + 2 * r(qb) + 2 * r(kb) + r(sb)
+    assert gqa.gqa_workspace_size_host(dims(batch=0), 64, 0) == 0
+    assert gqa.gqa_workspace_size_host(dims(seq_len=8), 7, 0) == 0
+    # checks the host can make come first, in gqa_forward's order
+    assert call_host(dims(batch=0)) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call_host(d, key=None, value=None) == gqa.GQA_ERR_UNSUPPORTED
+    for bad in (dict(query=None), dict(output=None), dict(seqlens_k=None), dict(key=None),
+                dict(query=P["q"] + 8), dict(seqlens_k=P["seq"] + 2), dict(workspace=None),
+                dict(workspace_bytes=need - 1), dict(workspace=P["ws"] + 8)):
+        assert call_host(d, **{"workspace_bytes": need, **bad}) == gqa.GQA_ERR_INVALID_ARGUMENT, bad
+    # the fake addresses are not page-locked host memory: rejected before any launch
+    assert call_host(d, workspace_bytes=need) == gqa.GQA_ERR_INVALID_ARGUMENT
