@@ -193,9 +193,11 @@ gqa_status_t gqa_decode_noalloc(const gqa_dims_t* dims,
  *
  * The call enqueues three stages on `stream`: a copy kernel that reads the
  * inputs from host memory into the workspace, gqa_forward's kernels on those
- * copies, and a copy kernel that writes the output to host memory.  The
- * output is valid once the stream reaches that point (e.g. after
- * cudaStreamSynchronize).  The caller must not change the host inputs, or
+ * copies, and a copy kernel that writes the output to host memory.  On the
+ * decode path (seq_len 1, head_size 128, at most 16 query heads per KV head)
+ * the attention kernel stores the output rows straight into the host output
+ * and the last stage is not needed.  The output is valid once the stream
+ * reaches the end of the call (e.g. after cudaStreamSynchronize).  The caller must not change the host inputs, or
  * read the host output, before then.  Error behaviour is gqa_forward's.
  */
 gqa_status_t gqa_forward_host(const gqa_dims_t* dims,

@@ -246,13 +246,15 @@ namespace {
 
 // gqa_forward with optional staging copies around the step: stage_in runs
 // after every check has passed and before the step's kernels, stage_out
-// after them.
+// after them.  With direct_out set, the decode kernel (whose output is plain
+// stores) writes the output there and stage_out is skipped.
 gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
                           const void* past_key, const void* past_value, void* present_key, void* present_value,
                           const int32_t* seqlens_k, int32_t total_sequence_length, const void* cos_cache,
                           const void* sin_cache, float scale, int32_t local_window_size,
                           const void* attention_bias, void* output, void* workspace, size_t workspace_bytes,
-                          void* stream, const StageList* stage_in, const StageList* stage_out) {
+                          void* stream, const StageList* stage_in, const StageList* stage_out,
+                          void* direct_out) {
   gqa_status_t st = check_dims(dims);
   if (st != GQA_OK) return st;
   const int B = dims->batch, S = dims->seq_len, H = dims->num_heads, Hkv = dims->kv_num_heads;
@@ -310,6 +312,10 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   a.err = err;
   a.num_sms = nsm;
 
+  if (direct_out && pl.path == Path::kDecode) {
+    a.out = direct_out;
+    stage_out = nullptr;
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = stage_in ? launch_stage(*stage_in, a.stream, nsm) : cudaSuccess;
   if (e != cudaSuccess) return GQA_ERR_CUDA;
@@ -379,7 +385,7 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
                          void* stream) {
   return forward_impl(dims, query, key, value, past_key, past_value, present_key, present_value, seqlens_k,
                       total_sequence_length, cos_cache, sin_cache, scale, local_window_size, attention_bias, output,
-                      workspace, workspace_bytes, stream, nullptr, nullptr);
+                      workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
 }
 
 size_t gqa_workspace_size_host(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size) {
@@ -421,7 +427,8 @@ gqa_status_t gqa_forward_host(const gqa_dims_t* dims, const void* query, const v
   out.n = 1;
   return forward_impl(dims, ws + h.q, ws + h.k, ws + h.v, past_key, past_value, present_key, present_value,
                       reinterpret_cast<const int32_t*>(ws + h.s), total_sequence_length, cos_cache, sin_cache,
-                      scale, local_window_size, attention_bias, ws + h.o, workspace, h.base, stream, &in, &out);
+                      scale, local_window_size, attention_bias, ws + h.o, workspace, h.base, stream, &in, &out,
+                      dout);
 }
 
 gqa_status_t gqa_check_device_status(void* stream) {
