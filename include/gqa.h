@@ -72,6 +72,8 @@ typedef struct {
   int32_t cos_cache_rows;     /* rows of cos/sin caches; ignored when cos_cache is NULL */
   int32_t bias_batch;         /* 1 or B; ignored when attention_bias is NULL */
   int32_t bias_heads;         /* 1 or H; ignored when attention_bias is NULL */
+  int32_t past_seq_len;       /* Mp: slots of past_key/past_value, 0 <= Mp <= M; read only
+                                 when past_key is not present_key (non-shared binding) */
 } gqa_dims_t;
 
 /*
@@ -80,11 +82,22 @@ typedef struct {
  *   dims             host: problem dimensions (above).
  *   query            device, T [B, S, H*D]   new query rows (heads contiguous per token).
  *   key, value       device, T [B, S, Hkv*D] new key/value rows.
- *   past_key         device, T [B, Hkv, M, D] the shared buffer.  It must be the same
- *   present_key      pointer as present_key (and past_value as present_value): the
- *   past_value       operator's shared past/present binding.  Different pointers
- *   present_value    return GQA_ERR_UNSUPPORTED.  Only slots [P_b, P_b + S) of each
- *                    (b, KV head) are written; every other slot keeps its bits.
+ *   past_key         device, T.  Two bindings ("Clarification about GroupQueryAttention
+ *   present_key      behavior": the quoted past_key text and ZackyLake's summary):
+ *   past_value       - shared: past_key == present_key and past_value == present_value,
+ *   present_value      one buffer [B, Hkv, M, D] of max_sequence_length slots.  Only
+ *                      slots [P_b, P_b + S) of each (b, KV head) are written; every
+ *                      other slot keeps its bits.
+ *                    - non-shared: four distinct buffers, past [B, Hkv, Mp, D]
+ *                      (Mp = dims->past_seq_len) and present [B, Hkv, M, D].  The
+ *                      present becomes past + new: slots [0, P_b) are copied from the
+ *                      past, slots [P_b, P_b + S) get the new rows, later slots keep
+ *                      their bits, and attention runs over the present.  The past is
+ *                      not written.  A sequence with P_b > Mp records
+ *                      GQA_ERR_INVALID_ARGUMENT on the device; its present slots below
+ *                      P_b are not copied.
+ *                    Only one of the two pairs equal (or a past buffer equal to the
+ *                    other present buffer) returns GQA_ERR_INVALID_ARGUMENT.
  *   seqlens_k        device, int32 [B]: past length P_b of each sequence (0 = empty).
  *   total_sequence_length  host scalar: an upper bound on P_b + S for every b and the
  *                    last dimension of attention_bias.  Must be >= S.  Larger than M:

@@ -118,6 +118,24 @@ def rotary(x_bits: np.ndarray, pos: np.ndarray, cos_bits: np.ndarray, sin_bits: 
 
 
 # ---------------------------------------------------------------------------
+# Step 0, non-shared binding only: the present state starts as the past
+# ([ORT], ZackyLake's summary 2b: when past and present are different tensors,
+# present is past + new; [MLIR] pad+scatter: the past rows come first and the
+# new rows are scattered after them at seqlens_k).
+# ---------------------------------------------------------------------------
+def present_from_past(present_bits: np.ndarray, past_bits: np.ndarray, seqlens_k: np.ndarray) -> np.ndarray:
+    """Return a copy of present [B, Hkv, M, D] whose slots [0, seqlens_k[b])
+    of every KV head hold the same slots of past [B, Hkv, Mp, D].  Every
+    other slot keeps its bits (the new rows land after the past ones in
+    step 2)."""
+    out = present_bits.copy()
+    for b in range(present_bits.shape[0]):
+        n = int(seqlens_k[b])
+        out[b, :, :n, :] = past_bits[b, :, :n, :]
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Step 2: scatter-append into the shared buffer ([MLIR]; [ORT] quoted text).
 # ---------------------------------------------------------------------------
 def scatter_append(buf_bits: np.ndarray, new_bits: np.ndarray, seqlens_k: np.ndarray) -> np.ndarray:
@@ -207,8 +225,15 @@ def check_lengths(seqlens_k, seq_len, max_seq_len, total_sequence_length) -> int
 
 def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length,
                 cos_cache, sin_cache, num_heads, kv_num_heads, scale, local_window_size,
-                attention_bias, dtype, batches=None, heads=None, interleaved=False):
+                attention_bias, dtype, batches=None, heads=None, interleaved=False,
+                past_key=None, past_value=None):
     """Returns (status, out, k_buf_new, v_buf_new).
+
+    Shared binding (past_key/past_value None): k_buf/v_buf are the one
+    past/present buffer.  Non-shared binding: past_key/past_value
+    [B, Hkv, Mp, D] hold the past, k_buf/v_buf are the present buffers as
+    they are on entry, and the present comes back as past + new (step 0); a
+    past length beyond Mp is an invalid argument.
 
     query [B, S, H*D], key/value [B, S, Hkv*D], k_buf/v_buf [B, Hkv, M, D],
     cos/sin [rows, D/2] or None (no rotary), attention_bias [Bb, Hb, S, total]
@@ -221,8 +246,13 @@ def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_lengt
     Hkv, M, D = k_buf.shape[1:]
     H = num_heads
     status = check_lengths(seqlens_k, S, M, total_sequence_length)
+    if status == STATUS_OK and past_key is not None and np.any(np.asarray(seqlens_k) > past_key.shape[2]):
+        status = STATUS_INVALID_ARGUMENT
     if status != STATUS_OK:
         return status, None, k_buf.copy(), v_buf.copy()
+    if past_key is not None:
+        k_buf = present_from_past(k_buf, past_key, seqlens_k)
+        v_buf = present_from_past(v_buf, past_value, seqlens_k)
     scale = float(np.float32(scale)) if scale > 0 else float(np.float32(1.0 / np.sqrt(D)))
     q = query.reshape(B, S, H, D)
     k = key.reshape(B, S, Hkv, D)

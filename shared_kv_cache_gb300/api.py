@@ -31,24 +31,26 @@ class Workspace:
 
 
 def dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache=None, attention_bias=None,
-             rotary_interleaved=0):
+             rotary_interleaved=0, past_seq_len=0):
     Bsz, S, HD = query.shape
     D = HD // num_heads
     M = k_buf.shape[2]
     bb, bh = (attention_bias.shape[0], attention_bias.shape[1]) if attention_bias is not None else (1, 1)
     rows = cos_cache.shape[0] if cos_cache is not None else 0
-    return B.make_dims(Bsz, S, num_heads, kv_num_heads, D, M, _DT[query.dtype], rotary_interleaved, rows, bb, bh)
+    return B.make_dims(Bsz, S, num_heads, kv_num_heads, D, M, _DT[query.dtype], rotary_interleaved, rows, bb, bh,
+                       past_seq_len)
 
 
 def _plan(workspace, host, query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias,
-          rotary_interleaved, total_sequence_length, local_window_size):
-    key_ = (host, tuple(query.shape), query.dtype, tuple(k_buf.shape), num_heads, kv_num_heads,
+          rotary_interleaved, total_sequence_length, local_window_size, past_seq_len=0):
+    key_ = (host, past_seq_len, tuple(query.shape), query.dtype, tuple(k_buf.shape), num_heads, kv_num_heads,
             None if cos_cache is None else cos_cache.shape[0],
             None if attention_bias is None else tuple(attention_bias.shape[:2]), rotary_interleaved,
             int(total_sequence_length), int(local_window_size))
     plan = workspace.plans.get(key_)
     if plan is None:
-        dims = dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias, rotary_interleaved)
+        dims = dims_for(query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias, rotary_interleaved,
+                        past_seq_len)
         size = B.gqa_workspace_size_host if host else B.gqa_workspace_size
         plan = (dims, size(dims, total_sequence_length, local_window_size))
         if len(workspace.plans) > 64:
@@ -59,18 +61,25 @@ def _plan(workspace, host, query, key, k_buf, num_heads, kv_num_heads, cos_cache
 
 def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, num_heads, kv_num_heads,
             cos_cache=None, sin_cache=None, scale=0.0, local_window_size=0, attention_bias=None,
-            output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
-    """One GroupQueryAttention step; k_buf/v_buf are updated in place (the
-    shared past/present binding).  Returns the output tensor [B, S, H*D]."""
+            output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0,
+            past_key=None, past_value=None):
+    """One GroupQueryAttention step.  k_buf/v_buf are updated in place: with
+    past_key/past_value None they are the shared past/present buffers;
+    otherwise they are the present buffers, which become past + new, and
+    past_key/past_value [B, Hkv, Mp, D] are read only.  Returns the output
+    tensor [B, S, H*D]."""
     workspace = workspace or Workspace()
+    mp = 0 if past_key is None else past_key.shape[2]
     dims, nbytes = _plan(workspace, False, query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias,
-                         rotary_interleaved, total_sequence_length, local_window_size)
+                         rotary_interleaved, total_sequence_length, local_window_size, mp)
     ws = workspace.get(nbytes, query.device)
     if output is None:
         output = torch.empty_like(query)
     if stream is None:
         stream = torch.cuda.current_stream(query.device)
-    st = B.gqa_forward(dims, query, key, value, k_buf, v_buf, k_buf, v_buf, seqlens_k, total_sequence_length,
+    pk = k_buf if past_key is None else past_key
+    pv = v_buf if past_value is None else past_value
+    st = B.gqa_forward(dims, query, key, value, pk, pv, k_buf, v_buf, seqlens_k, total_sequence_length,
                        cos_cache, sin_cache, scale, local_window_size, attention_bias, output, ws,
                        0 if ws is None else ws.numel(), stream)
     if st != B.GQA_OK:

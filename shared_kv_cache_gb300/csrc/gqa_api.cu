@@ -265,9 +265,17 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   if (!query || !key || !value || !past_key || !past_value || !present_key || !present_value || !seqlens_k ||
       !output)
     return GQA_ERR_INVALID_ARGUMENT;
-  // the shared binding: past and present are one tensor
-  if (past_key != present_key || past_value != present_value) return GQA_ERR_UNSUPPORTED;
+  // the binding: shared (past and present are one tensor) or non-shared
+  // (four distinct buffers; the present becomes past + new)
+  const bool shared = past_key == present_key && past_value == present_value;
   if (present_key == present_value) return GQA_ERR_INVALID_ARGUMENT;
+  if (!shared) {
+    if (past_key == present_key || past_value == present_value || past_key == past_value ||
+        past_key == present_value || past_value == present_key)
+      return GQA_ERR_INVALID_ARGUMENT;
+    if (dims->past_seq_len < 0 || dims->past_seq_len > M) return GQA_ERR_INVALID_ARGUMENT;
+    if (misaligned(past_key) || misaligned(past_value)) return GQA_ERR_INVALID_ARGUMENT;
+  }
   if (misaligned(query) || misaligned(key) || misaligned(value) || misaligned(present_key) ||
       misaligned(present_value) || misaligned(output) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
     return GQA_ERR_INVALID_ARGUMENT;
@@ -318,6 +326,7 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = stage_in ? launch_stage(*stage_in, a.stream, nsm) : cudaSuccess;
+  if (e == cudaSuccess && !shared) e = launch_present_copy(a, past_key, past_value, dims->past_seq_len);
   if (e != cudaSuccess) return GQA_ERR_CUDA;
   switch (pl.path) {
     case Path::kDecode:

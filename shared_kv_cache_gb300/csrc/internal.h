@@ -60,6 +60,9 @@ int device_smem_per_sm();
 
 // Kernel launchers (each returns the launch's cudaError_t).
 cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot);
+// Non-shared binding: slots [0, past_b) of the present buffers (a.kbuf,
+// a.vbuf) copied from past buffers of Mp slots.
+cudaError_t launch_present_copy(const ForwardArgs& a, const void* past_k, const void* past_v, int Mp);
 cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src);
 // Split-KV decode with a static partition and a separate combine kernel
 // (partials f32 [P, 2, G, D] and [P, 2, G, 2]; used by gqa_decode_noalloc).

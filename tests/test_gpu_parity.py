@@ -11,7 +11,7 @@ import oracle
 import shared_kv_cache_gb300 as gqa
 from shared_kv_cache_gb300 import workloads as W
 
-from gqa_cases import compare, run_cuda, run_oracle
+from gqa_cases import compare, run_cuda, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -180,3 +180,76 @@ def test_decode_repeat_is_idempotent():
 ])
 def test_prefill_cases(kw):
     check(custom(**kw))
+
+
+# ---------------------------------------------------------------------------
+# Non-shared binding: separate past [B, Hkv, Mp, D] and present buffers; the
+# present becomes past + new
+# ---------------------------------------------------------------------------
+def _split(inp, Mp, seed):
+    """Moves the case's past rows into separate past buffers of Mp slots
+    (later slots random: not part of the past) and makes the present buffers
+    all sentinel."""
+    w = inp["workload"]
+    gen = torch.Generator().manual_seed(seed)
+    past = {}
+    for name in ("k_buf", "v_buf"):
+        pk = torch.randn(w.batch, w.kv_num_heads, Mp, w.head_size, generator=gen).to(W.DTYPES[w.dtype])
+        for b, n in enumerate(inp["seqlens_k"].tolist()):
+            pk[b, :, :min(n, Mp)] = inp[name][b, :, :min(n, Mp)]
+        past[name] = pk
+        fresh = torch.empty(inp[name].shape, dtype=torch.int16).fill_(W.SENTINEL_BITS[w.dtype])
+        inp[name] = fresh.view(W.DTYPES[w.dtype])
+    return past
+
+
+def _run_cuda_split(inp, past):
+    w = inp["workload"]
+    d = to_device(inp)
+    pk, pv = past["k_buf"].cuda(), past["v_buf"].cuda()
+    out = torch.full_like(d["query"], float("nan"))
+    bias = d["attention_bias"]
+    dims = gqa.make_dims(w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len, w.dtype, 0,
+                         d["cos"].shape[0], 1 if bias is None else bias.shape[0],
+                         1 if bias is None else bias.shape[1], past_seq_len=pk.shape[2])
+    total = inp["total_sequence_length"]
+    ws = torch.empty(max(gqa.gqa_workspace_size(dims, total, inp["local_window_size"]), 256), dtype=torch.uint8,
+                     device="cuda")
+    st = gqa.gqa_forward(dims, d["query"], d["key"], d["value"], pk, pv, d["k_buf"], d["v_buf"], d["seqlens_k"],
+                         total, d["cos"], d["sin"], inp["scale"], inp["local_window_size"], bias, out, ws,
+                         ws.numel(), None)
+    dst = gqa.gqa_check_device_status(None)
+    return (st, dst, out.cpu(), d["k_buf"].cpu(), d["v_buf"].cpu()), (pk.cpu(), pv.cpu())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999), seed=81),   # decode kernel
+    dict(dtype="fp16", B=2, S=64, H=8, Hkv=2, D=128, M=512, past=(0, 300), bias=(1, 1), seed=82),  # tcgen05 prefill
+    dict(dtype="fp16", B=3, S=5, H=8, Hkv=2, D=64, M=256, past=(0, 17, 200), seed=83),      # generic path
+])
+def test_non_shared_binding(kw):
+    """The present buffers come back as past + new (bit for bit), the past
+    buffers unchanged, and the output matches the oracle."""
+    inp = custom(**kw)
+    Mp = min(kw["M"], max(kw["past"]) + 7)
+    past = _split(inp, Mp, seed=kw["seed"] + 500)
+    past_bits = {n: W.bits(t).copy() for n, t in past.items()}
+    res, (pk, pv) = _run_cuda_split(inp, past)
+    ref = run_oracle(inp, past_key=past_bits["k_buf"], past_value=past_bits["v_buf"])
+    compare(inp, res, ref)
+    assert np.array_equal(W.bits(pk), past_bits["k_buf"]) and np.array_equal(W.bits(pv), past_bits["v_buf"])
+
+
+def test_non_shared_past_shorter_than_a_length_records_an_error():
+    """A sequence whose past length is beyond the past's Mp slots records
+    GQA_ERR_INVALID_ARGUMENT and its present slots below that length are not
+    copied; the past is not written."""
+    inp = custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999), seed=84)
+    past = _split(inp, 600, seed=584)
+    past_bits = {n: W.bits(t).copy() for n, t in past.items()}
+    (st, dst, _, kb, vb), (pk, pv) = _run_cuda_split(inp, past)
+    assert st == gqa.GQA_OK and dst == gqa.GQA_ERR_INVALID_ARGUMENT
+    sentinel = W.SENTINEL_BITS["bf16"]
+    assert np.all(W.bits(kb)[2, :, :999] == sentinel) and np.all(W.bits(vb)[2, :, :999] == sentinel)
+    assert np.array_equal(W.bits(kb)[1, :, :517], past_bits["k_buf"][1, :, :517])
+    assert np.array_equal(W.bits(pk), past_bits["k_buf"]) and np.array_equal(W.bits(pv), past_bits["v_buf"])

@@ -80,9 +80,24 @@ def test_overflow_rejected_before_launch(lib):
     assert call(dims(max_seq_len=4096, seq_len=128), total=4128) == gqa.GQA_ERR_KV_OVERFLOW
 
 
-def test_shared_binding_required(lib):
-    assert call(dims(), present_key=P["kb"] + 4096) == gqa.GQA_ERR_UNSUPPORTED
-    assert call(dims(), present_value=P["vb"] + 4096) == gqa.GQA_ERR_UNSUPPORTED
+def test_binding_checks(lib):
+    """Shared binding (both pairs equal) or non-shared (four distinct
+    buffers); every call below breaks a rule and is rejected before any
+    launch."""
+    PK, PV = 0x200000, 0x300000   # separate present buffers (fake addresses)
+    # one pair shared and the other not
+    assert call(dims(), present_key=P["kb"] + 4096) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), present_value=P["vb"] + 4096) == gqa.GQA_ERR_INVALID_ARGUMENT
+    ns = dict(present_key=PK, present_value=PV)
+    # a past buffer that is another buffer of the call
+    assert call(dims(past_seq_len=64), past_key=PV, **ns) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(past_seq_len=64), past_value=PK, **ns) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(past_seq_len=64), past_value=P["kb"], **ns) == gqa.GQA_ERR_INVALID_ARGUMENT
+    # the past's slot count outside [0, M]
+    assert call(dims(past_seq_len=129, max_seq_len=128), **ns) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(past_seq_len=-1), **ns) == gqa.GQA_ERR_INVALID_ARGUMENT
+    # a misaligned past buffer
+    assert call(dims(past_seq_len=64), past_key=P["kb"] + 8, **ns) == gqa.GQA_ERR_INVALID_ARGUMENT
 
 
 def test_pointer_checks(lib):

@@ -476,3 +476,73 @@ def test_overflow_returns_error_and_leaves_buffers():
     # a length beyond total_sequence_length but inside the buffer is invalid
     w, inp = _small_case(M=24, past=(0, 5, 13), seed=113)
     assert _run_oracle(w, inp, total_sequence_length=16)[0] == oracle.STATUS_INVALID_ARGUMENT
+
+
+# ---------------------------------------------------------------------------
+# Non-shared binding: separate past and present buffers, present = past + new
+# ---------------------------------------------------------------------------
+def _split_binding(w, inp, Mp, seed):
+    """The case's past rows moved into separate past buffers of Mp slots
+    (slots from past_b on hold other random rows, not part of the past) and
+    present buffers that start as the sentinel."""
+    B, Hkv, D = w.batch, w.kv_num_heads, w.head_size
+    gen = torch.Generator().manual_seed(seed)
+    past, present = {}, {}
+    for name in ("k_buf", "v_buf"):
+        pk = torch.randn(B, Hkv, Mp, D, generator=gen).to(W.DTYPES[w.dtype])
+        for b, n in enumerate(inp["seqlens_k"].tolist()):
+            pk[b, :, :min(n, Mp)] = inp[name][b, :, :min(n, Mp)]
+        past[name] = W.bits(pk)
+        present[name] = np.full(W.bits(inp[name]).shape, W.SENTINEL_BITS[w.dtype], dtype=np.uint16)
+    return past, present
+
+
+def _run_split(w, inp, past, present):
+    return _run_oracle(w, inp, k_buf=present["k_buf"], v_buf=present["v_buf"], past_key=past["k_buf"],
+                       past_value=past["v_buf"])
+
+
+def test_non_shared_present_is_past_then_new():
+    """Per sequence the present holds cat(past[:past_b], new rows) -- built
+    here with torch.cat from the raw value rows -- and every later slot keeps
+    its bits; the output is exactly the shared binding's on a buffer that
+    holds the same past."""
+    w, inp = _small_case(sentinel=True, seed=120)
+    B, S, Hkv, D = w.batch, w.seq_len, w.kv_num_heads, w.head_size
+    past, present = _split_binding(w, inp, Mp=max(inp["seqlens_k"].tolist()) + 3, seed=121)
+    st, out, kb, vb = _run_split(w, inp, past, present)
+    st2, out2, kb2, _ = _run_oracle(w, inp)
+    assert st == st2 == oracle.STATUS_OK
+    assert np.array_equal(out, out2)
+    new_v = inp["value"].view(torch.int16).reshape(B, S, Hkv, D)
+    for b, pb in enumerate(inp["seqlens_k"].tolist()):
+        L = pb + S
+        cat_v = torch.cat([torch.from_numpy(past["v_buf"][b, :, :pb].view(np.int16)), new_v[b].transpose(0, 1)], dim=1)
+        assert np.array_equal(vb[b, :, :L].view(np.int16), cat_v.numpy())
+        assert np.array_equal(kb[b, :, :L], kb2[b, :, :L])  # rotated keys as in the shared binding
+        assert np.all(kb[b, :, L:] == W.SENTINEL_BITS[w.dtype]) and np.all(vb[b, :, L:] == W.SENTINEL_BITS[w.dtype])
+
+
+def test_non_shared_ignores_past_beyond_its_length():
+    """Past slots from past_b on are not part of the past: changing them
+    changes neither the output nor the present."""
+    w, inp = _small_case(sentinel=True, seed=122)
+    Mp = max(inp["seqlens_k"].tolist()) + 5
+    past, present = _split_binding(w, inp, Mp, seed=123)
+    st, out, kb, vb = _run_split(w, inp, past, present)
+    for name in ("k_buf", "v_buf"):
+        for b, pb in enumerate(inp["seqlens_k"].tolist()):
+            past[name][b, :, pb:] ^= 0x1234
+    st2, out2, kb2, vb2 = _run_split(w, inp, past, present)
+    assert st == st2 == oracle.STATUS_OK
+    assert np.array_equal(out, out2) and np.array_equal(kb, kb2) and np.array_equal(vb, vb2)
+
+
+def test_non_shared_past_shorter_than_a_length_is_invalid():
+    w, inp = _small_case(sentinel=True, seed=124, past=(0, 5, 13))
+    past, present = _split_binding(w, inp, Mp=13, seed=125)
+    assert _run_split(w, inp, past, present)[0] == oracle.STATUS_OK     # past_b == Mp is fine
+    past, present = _split_binding(w, inp, Mp=12, seed=125)
+    st, out, kb, vb = _run_split(w, inp, past, present)
+    assert st == oracle.STATUS_INVALID_ARGUMENT and out is None
+    assert np.array_equal(kb, present["k_buf"]) and np.array_equal(vb, present["v_buf"])
