@@ -50,8 +50,8 @@ def parse():
     ap.add_argument("--workload", default=HEADLINE,
                     help="workload to time as the headline (default: the batched decode)")
     ap.add_argument("--quick", action="store_true",
-                    help="headline workload only: no burn-in, end-to-end leg, other workloads or CPU baseline "
-                         "(for profiler runs)")
+                    help="headline workload only: no burn-in, one end-to-end step, no other workloads or CPU "
+                         "baseline (for profiler runs)")
     return ap.parse_args()
 
 

@@ -167,7 +167,8 @@ const char* gqa_status_string(gqa_status_t status);
  * device array of 4 MiB inside the library (held by every GPU that loads it,
  * until exit; a 152-SM GB300 needs at most about 2.5 MB of it); a call that
  * would need more returns GQA_ERR_UNSUPPORTED before any launch, as do shapes
- * other than the decode shape above.  The function allocates nothing.
+ * other than the decode shape above and the non-shared binding (separate past
+ * and present buffers).  The function allocates nothing.
  *   - All calls on one device share that array and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose kernels
  *     can overlap on the GPU race on it: order them on one stream.
