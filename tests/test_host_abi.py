@@ -169,3 +169,47 @@ def test_host_entry_workspace_and_checks(lib):
         assert call_host(d, **{"workspace_bytes": need, **bad}) == gqa.GQA_ERR_INVALID_ARGUMENT, bad
     # the fake addresses are not page-locked host memory: rejected before any launch
     assert call_host(d, workspace_bytes=need) == gqa.GQA_ERR_INVALID_ARGUMENT
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_workspace_plan_generic_path():
+    # head size other than 128: the append kernel writes the rotated queries
+    # to the workspace, T [B, S, H, D]
+    d = dims(batch=3, seq_len=5, num_heads=8, kv_num_heads=2, head_size=64, max_seq_len=256)
+    assert gqa.gqa_workspace_size(d, 205, 0) == _r256(3 * 5 * 8 * 64 * 2)
+
+
+def test_workspace_plan_prefill_splits():
+    # tensor-core prefill: a grid of at least two CTAs per SM (B * Hkv *
+    # ceil(G / 2) * query tiles >= 2 * 152) needs no scratch
+    big = dims(batch=4, seq_len=2048, num_heads=32, kv_num_heads=8, head_size=128, max_seq_len=4096)
+    assert gqa.gqa_workspace_size(big, 2048, 0) == 0
+    # a smaller grid cuts each query tile's key range into
+    # min(ceil(3 * 152 / CTAs), key tiles + 1) pieces and keeps fp32 partials
+    # (rows = CTAs x pieces x 2 query tiles x 128 rows; D floats plus (m, l) each)
+    small = dims(batch=8, seq_len=128, num_heads=32, kv_num_heads=8, head_size=128, max_seq_len=4096)
+    ctas = 8 * 8 * 2 * 1
+    pieces = min(-(-3 * 152 // ctas), 4096 // 128 + 1)
+    assert pieces == 4
+    rows = ctas * pieces * 2 * 128
+    assert gqa.gqa_workspace_size(small, 4096, 0) == _r256(_r256(rows * 128 * 4) + rows * 2 * 4)
+    # few key tiles bound the pieces
+    short = dims(batch=1, seq_len=128, num_heads=8, kv_num_heads=8, head_size=128, max_seq_len=4096)
+    ctas = 1 * 8 * 1 * 1
+    pieces = min(-(-3 * 152 // ctas), 256 // 128 + 1)
+    assert pieces == 3
+    rows = ctas * pieces * 2 * 128
+    assert gqa.gqa_workspace_size(short, 256, 0) == _r256(_r256(rows * 128 * 4) + rows * 2 * 4)
+
+
+def test_workspace_plan_decode_large_group():
+    # 16 query heads per KV head: one decode CTA per SM (its shared memory
+    # does not fit twice), so 2 x 2 x 152 partial slots of 16 x (128 + 2)
+    # floats, one arrival counter each and the chunk ticket
+    d = dims(seq_len=1, head_size=128, num_heads=128, kv_num_heads=8, batch=4, max_seq_len=8192)
+    slots = 2 * 2 * 152
+    want = _r256(8 * (1 + slots)) + _r256(slots * 16 * 128 * 4) + _r256(slots * 16 * 2 * 4)
+    assert gqa.gqa_workspace_size(d, 8192, 0) == want
