@@ -89,21 +89,26 @@ def forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, n
 
 def forward_host(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length, num_heads, kv_num_heads,
                  cos_cache=None, sin_cache=None, scale=0.0, local_window_size=0, attention_bias=None,
-                 output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0):
+                 output=None, workspace: Optional[Workspace] = None, stream=None, rotary_interleaved=0,
+                 past_key=None, past_value=None):
     """forward() with query/key/value/seqlens_k and the output as pinned CPU
-    tensors (gqa_forward_host); k_buf, v_buf, the caches and the bias stay on
-    the device.  The returned output is valid once `stream` has reached the
-    end of the step (synchronise it before reading)."""
+    tensors (gqa_forward_host); k_buf, v_buf (and past_key/past_value in the
+    non-shared binding), the caches and the bias stay on the device.  The
+    returned output is valid once `stream` has reached the end of the step
+    (synchronise it before reading)."""
     workspace = workspace or Workspace()
     dev = k_buf.device
+    mp = 0 if past_key is None else past_key.shape[2]
     dims, nbytes = _plan(workspace, True, query, key, k_buf, num_heads, kv_num_heads, cos_cache, attention_bias,
-                         rotary_interleaved, total_sequence_length, local_window_size)
+                         rotary_interleaved, total_sequence_length, local_window_size, mp)
     ws = workspace.get(nbytes, dev)
     if output is None:
         output = torch.empty(query.shape, dtype=query.dtype, pin_memory=True)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    st = B.gqa_forward_host(dims, query, key, value, k_buf, v_buf, k_buf, v_buf, seqlens_k, total_sequence_length,
+    pk = k_buf if past_key is None else past_key
+    pv = v_buf if past_value is None else past_value
+    st = B.gqa_forward_host(dims, query, key, value, pk, pv, k_buf, v_buf, seqlens_k, total_sequence_length,
                             cos_cache, sin_cache, scale, local_window_size, attention_bias, output, ws,
                             0 if ws is None else ws.numel(), stream)
     if st != B.GQA_OK:
