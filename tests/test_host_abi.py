@@ -213,3 +213,28 @@ def test_workspace_plan_decode_large_group():
     slots = 2 * 2 * 152
     want = _r256(8 * (1 + slots)) + _r256(slots * 16 * 128 * 4) + _r256(slots * 16 * 2 * 4)
     assert gqa.gqa_workspace_size(d, 8192, 0) == want
+
+
+def _header_text():
+    text = open(os.path.join(ROOT, "include", "gqa.h")).read()
+    return re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+
+
+def test_dims_struct_matches_header():
+    """The ctypes mirror of gqa_dims_t has the header's fields, in order, all
+    int32 (so the layout is the same on both sides)."""
+    body = re.search(r"typedef struct \{(.*?)\}\s*gqa_dims_t;", _header_text(), flags=re.S).group(1)
+    fields = re.findall(r"int32_t\s+(\w+)\s*;", body)
+    assert [f for f, _ in gqa.gqa_dims_t._fields_] == fields
+    assert all(t is ctypes.c_int32 for _, t in gqa.gqa_dims_t._fields_)
+    assert ctypes.sizeof(gqa.gqa_dims_t) == 4 * len(fields)
+
+
+def test_bound_argument_counts_match_header(lib):
+    """Every function the binding declares takes as many arguments as the
+    header's prototype."""
+    text = _header_text()
+    for name in gqa.EXPORTED:
+        proto = re.search(r"\b" + name + r"\s*\((.*?)\)\s*;", text, flags=re.S).group(1)
+        n = 0 if proto.strip() in ("", "void") else proto.count(",") + 1
+        assert len(getattr(lib, name).argtypes) == n, name
