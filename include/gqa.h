@@ -88,7 +88,8 @@ typedef struct {
  *   present_value      one buffer [B, Hkv, M, D] of max_sequence_length slots.  Only
  *                      slots [P_b, P_b + S) of each (b, KV head) are written; every
  *                      other slot keeps its bits.
- *                    - non-shared: four distinct buffers, past [B, Hkv, Mp, D]
+ *                    - non-shared: four distinct, non-overlapping buffers (only
+ *                      pointer equality is checked), past [B, Hkv, Mp, D]
  *                      (Mp = dims->past_seq_len) and present [B, Hkv, M, D].  The
  *                      present becomes past + new: slots [0, P_b) are copied from the
  *                      past, slots [P_b, P_b + S) get the new rows, later slots keep
