@@ -136,10 +136,12 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims,
 
 /*
  * gqa_workspace_size -- bytes of device scratch gqa_forward needs for these
- * dims, total_sequence_length and local_window_size (rotated queries for the
- * prefill kernels, per-split partial results for split-KV decode).  The
- * figure is for the current device and covers calls with or without rotary
- * embedding.  Returns 0 for invalid dims (and when no scratch is needed).
+ * dims, total_sequence_length and local_window_size: rotated queries for the
+ * generic kernel (head sizes other than 128), key-range partials for a
+ * tensor-core prefill grid of fewer than two CTAs per SM, and split-KV
+ * partials with their counters for decode.  The figure is for the current
+ * device and covers calls with or without rotary embedding and either
+ * binding.  Returns 0 for invalid dims (and when no scratch is needed).
  */
 size_t gqa_workspace_size(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size);
 
