@@ -9,10 +9,12 @@ import oracle
 import shared_kv_cache_gb300 as gqa
 from shared_kv_cache_gb300 import workloads as W
 
-# Attention output tolerance (max abs against the oracle's float64 result):
-# 2e-3 for fp16, 1e-2 for bf16, but never finer than one unit in the last
-# place of the output type at the reference value -- an output stored in T
-# cannot resolve more than that (for |o| >= 2 in bf16, >= 4 in fp16).
+# Attention output tolerance: max-abs 2e-3 for fp16 and 1e-2 for bf16 against
+# the oracle's float64 result.  A T output is at best the correctly rounded
+# value, at most half a unit in the last place (ulp) from the exact one; where
+# that half ulp alone exceeds the tolerance (bf16 |o| >= 4, fp16 |o| >= 8) no
+# T output can meet it, and there the output must be faithfully rounded
+# instead: less than one ulp of T from the exact value.
 TOL = {"fp16": 2e-3, "bf16": 1e-2}
 
 
@@ -42,6 +44,29 @@ def run_cuda(inp: dict, stream=None, total=None, workspace_pad=0):
                          d["attention_bias"], out, ws, ws.numel(), stream)
     dst = gqa.gqa_check_device_status(stream)
     return st, dst, out.cpu(), d["k_buf"].cpu(), d["v_buf"].cpu()
+
+
+def custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999), seed=7, bias=None,
+           window=0, total=None, rotary=True, interleaved=0, sentinel=True):
+    """A seeded case of any shape: per-sequence past lengths `past`, past rows
+    N(0, 1), other slots the NaN sentinel; bias (Bb, Hb) ~ N(0, 0.5)."""
+    w = W.Workload("custom", dtype, B, S, H, Hkv, D, M, 0, 0, bias_shape=bias, local_window_size=window,
+                   total_sequence_length=total, rotary=rotary, seed=seed)
+    inp = W.make_inputs(w, sentinel=sentinel, fill_past=False)
+    inp["seqlens_k"] = torch.tensor(past, dtype=torch.int32)
+    gen = torch.Generator().manual_seed(seed + 1000)
+    for name in ("k_buf", "v_buf"):
+        for b, n in enumerate(past):
+            if n > 0:
+                inp[name][b, :, :n] = torch.randn(Hkv, n, D, generator=gen).to(W.DTYPES[dtype])
+    t = total if total is not None else max(past) + S
+    inp["total_sequence_length"] = t
+    if rotary:
+        inp["cos"], inp["sin"] = W.rotary_cache(max(t, M), D, dtype)
+    if bias is not None:
+        inp["attention_bias"] = (torch.randn(bias[0], bias[1], S, t, generator=gen) * 0.5).to(W.DTYPES[dtype])
+    inp["rotary_interleaved"] = interleaved
+    return inp
 
 
 def run_oracle(inp: dict, batches=None, heads=None, **kw):
@@ -81,15 +106,32 @@ def compare(inp: dict, cuda_res, oracle_res, heads=None, batches=None):
     r = ref[bs][:, :, hs]
     assert np.all(np.isfinite(g)), "non-finite output"
     e = np.abs(g - r)
-    bound = np.maximum(TOL[w.dtype], ulp(r, w.dtype))
-    worst = np.unravel_index(np.argmax(e - bound), e.shape)
-    assert np.all(e <= bound), (f"error {e[worst]:.4e} > bound {bound[worst]:.4e} at {worst}: "
-                                f"gpu {g[worst]:.6f} oracle {r[worst]:.6f}")
+    ok, n_floor = within_tolerance(e, r, w.dtype)
+    if not ok.all():
+        u = ulp(r, w.dtype)
+        excess = np.where(ok, -np.inf, e - np.where(0.5 * u > TOL[w.dtype], u, TOL[w.dtype]))
+        worst = np.unravel_index(np.argmax(excess), e.shape)
+        raise AssertionError(f"{int((~ok).sum())} outputs out of tolerance; worst error {e[worst]:.4e} at {worst}: "
+                             f"gpu {g[worst]:.6f} oracle {r[worst]:.6f} (ulp {u[worst]:.3e})")
+    if n_floor:
+        print(f"[{w.name}] {n_floor} of {e.size} outputs above the range where {TOL[w.dtype]} is attainable "
+              f"(checked for faithful rounding)")
     return float(e.max())
+
+
+def within_tolerance(err, ref, dtype):
+    """(ok mask, number of elements under the faithful-rounding rule).  Where
+    half an ulp of T at the reference fits in the tolerance, the error must be
+    within the tolerance; elsewhere it must be below one ulp."""
+    u = ulp(ref, dtype)
+    floor = 0.5 * u > TOL[dtype]
+    ok = np.where(floor, err < u, err <= TOL[dtype])
+    return ok, int(floor.sum())
 
 
 def ulp(x, dtype):
     """One unit in the last place of T at |x| (normal range)."""
     bits = 10 if dtype == "fp16" else 7
     ax = np.maximum(np.abs(x), np.finfo(np.float64).tiny)
-    return np.exp2(np.floor(np.log2(ax)) - bits)
+    _, e = np.frexp(ax)             # ax = m * 2^e, m in [0.5, 1): exact, unlike log2 near a power of two
+    return np.ldexp(1.0, e - 1 - bits)

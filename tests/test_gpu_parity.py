@@ -11,7 +11,7 @@ import oracle
 import shared_kv_cache_gb300 as gqa
 from shared_kv_cache_gb300 import workloads as W
 
-from gqa_cases import compare, run_cuda, run_oracle, to_device
+from gqa_cases import compare, custom, run_cuda, run_oracle, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -21,27 +21,6 @@ def _lib():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     gqa.load_library()
-
-
-def custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999), seed=7, bias=None,
-           window=0, total=None, rotary=True, interleaved=0, sentinel=True):
-    w = W.Workload("custom", dtype, B, S, H, Hkv, D, M, 0, 0, bias_shape=bias, local_window_size=window,
-                   total_sequence_length=total, rotary=rotary, seed=seed)
-    inp = W.make_inputs(w, sentinel=sentinel, fill_past=False)
-    inp["seqlens_k"] = torch.tensor(past, dtype=torch.int32)
-    gen = torch.Generator().manual_seed(seed + 1000)
-    for name in ("k_buf", "v_buf"):
-        for b, n in enumerate(past):
-            if n > 0:
-                inp[name][b, :, :n] = torch.randn(Hkv, n, D, generator=gen).to(W.DTYPES[dtype])
-    t = total if total is not None else max(past) + S
-    inp["total_sequence_length"] = t
-    if rotary:
-        inp["cos"], inp["sin"] = W.rotary_cache(max(t, M), D, dtype)
-    if bias is not None:
-        inp["attention_bias"] = (torch.randn(bias[0], bias[1], S, t, generator=gen) * 0.5).to(W.DTYPES[dtype])
-    inp["rotary_interleaved"] = interleaved
-    return inp
 
 
 def check(inp, heads=None, batches=None):
@@ -74,17 +53,19 @@ def test_decode_b16_full():
     check(W.make_inputs(W.CONFIGS["decode_b16"]))
 
 
-def test_prefill_2k_full_sampled_heads():
-    check(W.make_inputs(W.CONFIGS["prefill_2k"]), heads=[0, 7, 12, 31])
+def test_prefill_2k_full():
+    """Every head of every sequence (4 x 2048 rows x 32 heads)."""
+    check(W.make_inputs(W.CONFIGS["prefill_2k"]))
 
 
 def test_chunked_prefill_full_with_bias():
-    check(W.make_inputs(W.CONFIGS["chunked_prefill"]), heads=[0, 3, 17, 30])
+    check(W.make_inputs(W.CONFIGS["chunked_prefill"]))
 
 
 @pytest.mark.parametrize("name", ["long_decode", "long_decode_w4096"])
-def test_long_decode_full_sampled_heads(name):
-    check(W.make_inputs(W.CONFIGS[name]), heads=[0, 9, 37, 63])
+def test_long_decode_full(name):
+    """All 64 heads of all 8 sequences."""
+    check(W.make_inputs(W.CONFIGS[name]))
 
 
 def test_chunked_overflow_is_an_error_and_writes_nothing():
