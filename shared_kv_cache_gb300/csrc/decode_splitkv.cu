@@ -814,14 +814,10 @@ cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, float* part_o, floa
                  a.scale * kLog2e};
   const int smem = layout_for(G).total;
   auto kern = G <= 8 ? decode_kernel<T, 1> : decode_kernel<T, 2>;
-  static int attr_set[64][2] = {};  // dynamic shared memory set so far, per device and variant
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int vi = G <= 8 ? 0 : 1;
-  if (dev < 0 || dev >= 64 || attr_set[dev][vi] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<int> smem_set[2][kMaxDevices];  // limit set so far, per variant and device
+  {
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem, smem_set[G <= 8 ? 0 : 1]);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev][vi] = smem;
   }
   kern<<<plan.ctas, kThreads, smem, a.stream>>>(kmap, vmap, p);
   cudaError_t e = cudaGetLastError();

@@ -20,8 +20,6 @@ __device__ int g_error_word;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 int current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -99,6 +97,19 @@ int smem_per_sm() {
 }
 
 }  // namespace
+
+cudaError_t set_smem_limit(const void* func, int bytes, std::atomic<int>* cache) {
+  const int dev = current_device();
+  if (dev >= 0 && cache[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0) {
+    // keep the largest limit set (two threads may race here; both set valid limits)
+    int cur = cache[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !cache[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+    }
+  }
+  return e;
+}
 
 // Accessors for other translation units of the library.
 int* device_error_word() { return error_word_ptr(); }

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gqa.h"
 
 namespace gqa {
@@ -94,6 +96,12 @@ struct StageList {
   int n = 0;
 };
 cudaError_t launch_stage(const StageList& l, cudaStream_t stream, int num_sms);
+
+// Raises the dynamic shared-memory limit of kernel `func` to `bytes` on the
+// current device, once: `cache` is the caller's per-device record of the
+// limit set so far (kMaxDevices entries, safe for concurrent host threads).
+constexpr int kMaxDevices = 64;
+cudaError_t set_smem_limit(const void* func, int bytes, std::atomic<int>* cache);
 
 // Tensor-map encoding through the driver entry point (no libcuda link).
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* base,

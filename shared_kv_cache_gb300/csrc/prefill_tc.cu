@@ -698,14 +698,11 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   p.n_split = n_split;
   p.scale_log2 = a.scale * kLog2e;
   auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
-  static bool attr_set[64][2] = {};  // per device and instantiation
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int vi = a.bias ? 1 : 0;
-  if (dev < 0 || dev >= 64 || !attr_set[dev][vi]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  static std::atomic<int> smem_set[2][kMaxDevices];  // limit set so far, per instantiation and device
+  {
+    const cudaError_t e =
+        set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes, smem_set[a.bias ? 1 : 0]);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev][vi] = true;
   }
   const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
   kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, p);
