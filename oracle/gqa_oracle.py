@@ -9,7 +9,8 @@ Sources (page title, then the passage):
          discussion 29659): the shared past/present buffer of
          max_sequence_length (the quoted operator text), the failure when the
          buffer has no room (tianleiwu's reply), the attention_bias shape and
-         the sliding-window cache capacity (the follow-up questions).
+         the sliding-window cache that keeps only the min(total, capacity)
+         most recent tokens contiguously (ZackyLake's SWA follow-up).
   [MLIR] "[TorchOnnxToTorch] Add pad+scatter KV cache and mask to GQA"
          (torch-mlir PR 4471), the PR description: position ids = arange plus
          the past length from seqlens_k, key rotary on kv_num_heads, seqlens_k
@@ -205,18 +206,105 @@ def attention(q_bits, k_buf, v_buf, seqlens_k, num_heads, kv_num_heads, scale, w
 
 
 # ---------------------------------------------------------------------------
+# Packed QKV input: one tensor holding every token's query, key and value
+# heads.
+# ---------------------------------------------------------------------------
+def unpack_qkv(packed_bits: np.ndarray, num_heads: int, kv_num_heads: int):
+    """query [B, S, (H + 2 Hkv) * D] in the packed form -> (query [B, S, H*D],
+    key [B, S, Hkv*D], value [B, S, Hkv*D]).  Each token's row is read as
+    [heads, head_size] with the head index outer ([MLIR] PR description: the
+    [batch, seq, hidden] input is reshaped to [batch, seq, heads, head_size]):
+    heads [0, H) are the query heads, [H, H + Hkv) the key heads and
+    [H + Hkv, H + 2 Hkv) the value heads."""
+    B, S, width = packed_bits.shape
+    n = num_heads + 2 * kv_num_heads
+    D = width // n
+    x = packed_bits.reshape(B, S, n, D)
+    q = x[:, :, :num_heads].reshape(B, S, num_heads * D)
+    k = x[:, :, num_heads:num_heads + kv_num_heads].reshape(B, S, kv_num_heads * D)
+    v = x[:, :, num_heads + kv_num_heads:].reshape(B, S, kv_num_heads * D)
+    return q.copy(), k.copy(), v.copy()
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window cache with contiguous eviction ([ORT], ZackyLake's SWA
+# follow-up: the op keeps only the min(total_sequence_length, cache_capacity)
+# most recent tokens, contiguously).  Here the capacity is the buffer's
+# max_seq_len slots M, and seqlens_k[b] = P_b counts every token of the
+# sequence before the call (its absolute position), which may exceed M: the
+# buffer then holds the n_old = min(P_b, M) most recent of them, slot s
+# holding position P_b - n_old + s.
+# ---------------------------------------------------------------------------
+def cached_count(past: int, max_seq_len: int) -> int:
+    """Tokens of a sequence held in the buffer on entry: min(P_b, M)."""
+    return min(int(past), max_seq_len)
+
+
+def evict_keep_recent(buf_bits: np.ndarray, new_bits: np.ndarray, seqlens_k: np.ndarray) -> np.ndarray:
+    """Return a copy of buf [B, Hkv, M, D] in which, per sequence, the cached
+    tokens followed by the S new ones (new [B, S, Hkv, D]) are cut to their
+    n_keep = min(P_b + S, M) most recent, stored contiguously from slot 0.
+    Slots [n_keep, M) keep their bits."""
+    out = buf_bits.copy()
+    B, Hkv, M, D = buf_bits.shape
+    for b in range(B):
+        n_old = cached_count(seqlens_k[b], M)
+        seq = np.concatenate([buf_bits[b, :, :n_old, :], new_bits[b].transpose(1, 0, 2)], axis=1)
+        n_keep = min(int(seqlens_k[b]) + new_bits.shape[1], M)
+        out[b, :, :n_keep, :] = seq[:, seq.shape[1] - n_keep:, :]
+    return out
+
+
+def attention_evicting(q_bits, k_buf, v_buf, k_new, v_new, seqlens_k, num_heads, kv_num_heads, scale, window,
+                       bias_bits, dtype):
+    """Output [B, S, H, D] float64 of a call in the evicting mode: token i of
+    sequence b (position p = P_b + i) attends over the keys that exist for
+    the call -- the n_old cached tokens (positions P_b - n_old ...) and the S
+    new ones -- that are causal (j <= p) and, with W > 0, among the W most
+    recent (j > p - W).  The bias is read at the absolute key position j.
+    k_buf/v_buf [B, Hkv, M, D] are the buffers on entry; k_new/v_new
+    [B, S, Hkv, D] the new rows (keys rotated)."""
+    B, S, H, D = q_bits.shape
+    M = k_buf.shape[2]
+    G = num_heads // kv_num_heads
+    q = t_to_f64(q_bits, dtype)
+    bias = None if bias_bits is None else t_to_f64(bias_bits, dtype)
+    out = np.full((B, S, H, D), np.nan)
+    for b in range(B):
+        past = int(seqlens_k[b])
+        n_old = cached_count(past, M)
+        K = t_to_f64(np.concatenate([k_buf[b, :, :n_old], k_new[b].transpose(1, 0, 2)], axis=1), dtype)
+        V = t_to_f64(np.concatenate([v_buf[b, :, :n_old], v_new[b].transpose(1, 0, 2)], axis=1), dtype)
+        kpos = past - n_old + np.arange(n_old + S)
+        p = past + np.arange(S)[:, None]
+        vis = kpos[None, :] <= p
+        if window > 0:
+            vis &= kpos[None, :] > p - window
+        for h in range(H):
+            kh = h // G
+            z = (q[b, :, h, :] @ K[kh].T) * scale
+            if bias is not None:
+                z = z + bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0][:, kpos]
+            z = np.where(vis, z, -np.inf)
+            e = np.exp(z - z.max(axis=1, keepdims=True))
+            out[b, :, h, :] = (e / e.sum(axis=1, keepdims=True)) @ V[kh]
+    return out
+
+
+# ---------------------------------------------------------------------------
 # The whole operator.
 # ---------------------------------------------------------------------------
-def check_lengths(seqlens_k, seq_len, max_seq_len, total_sequence_length) -> int:
+def check_lengths(seqlens_k, seq_len, max_seq_len, total_sequence_length, evict=False) -> int:
     """Step 4: the operator fails when the buffer has no room for the new
     tokens ([ORT], tianleiwu's reply).  A sequence whose past plus new tokens
     exceeds total_sequence_length (the last dimension of attention_bias) is an
-    invalid argument."""
-    if total_sequence_length > max_seq_len:
+    invalid argument.  In the evicting mode the buffer always has room (the
+    oldest tokens make way), so only the invalid-argument checks remain."""
+    if total_sequence_length > max_seq_len and not evict:
         return STATUS_KV_OVERFLOW
     status = STATUS_OK
     for pb in np.asarray(seqlens_k, dtype=np.int64):
-        if pb + seq_len > max_seq_len:
+        if pb + seq_len > max_seq_len and not evict:
             return STATUS_KV_OVERFLOW
         if pb < 0 or pb + seq_len > total_sequence_length:
             status = STATUS_INVALID_ARGUMENT
@@ -226,8 +314,13 @@ def check_lengths(seqlens_k, seq_len, max_seq_len, total_sequence_length) -> int
 def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_length,
                 cos_cache, sin_cache, num_heads, kv_num_heads, scale, local_window_size,
                 attention_bias, dtype, batches=None, heads=None, interleaved=False,
-                past_key=None, past_value=None):
+                past_key=None, past_value=None, evict=False):
     """Returns (status, out, k_buf_new, v_buf_new).
+
+    Packed QKV: key and value None, query [B, S, (H + 2 Hkv) * D] (see
+    unpack_qkv).  evict=True selects the sliding-window cache with
+    contiguous eviction (shared binding only; see evict_keep_recent and
+    attention_evicting); batches/heads are ignored there.
 
     Shared binding (past_key/past_value None): k_buf/v_buf are the one
     past/present buffer.  Non-shared binding: past_key/past_value
@@ -242,10 +335,14 @@ def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_lengt
     buffers come back unchanged and ``out`` is None.  scale <= 0 means
     1/sqrt(D); the scale is taken as a float32 value, as the operator's
     attribute is."""
+    if key is None and value is None:
+        query, key, value = unpack_qkv(query, num_heads, kv_num_heads)
+    if evict and past_key is not None:
+        raise ValueError("the evicting cache is defined for the shared binding only")
     B, S = query.shape[:2]
     Hkv, M, D = k_buf.shape[1:]
     H = num_heads
-    status = check_lengths(seqlens_k, S, M, total_sequence_length)
+    status = check_lengths(seqlens_k, S, M, total_sequence_length, evict)
     if status == STATUS_OK and past_key is not None and np.any(np.asarray(seqlens_k) > past_key.shape[2]):
         status = STATUS_INVALID_ARGUMENT
     if status != STATUS_OK:
@@ -261,6 +358,12 @@ def gqa_forward(query, key, value, k_buf, v_buf, seqlens_k, total_sequence_lengt
         pos = positions(seqlens_k, S)
         q = rotary(q, pos, cos_cache, sin_cache, dtype, interleaved)
         k = rotary(k, pos, cos_cache, sin_cache, dtype, interleaved)
+    if evict:
+        out = attention_evicting(q, k_buf, v_buf, k, v, seqlens_k, H, Hkv, scale, local_window_size,
+                                 attention_bias, dtype)
+        kb = evict_keep_recent(k_buf, k, seqlens_k)
+        vb = evict_keep_recent(v_buf, v, seqlens_k)
+        return STATUS_OK, out.reshape(B, S, H * D), kb, vb
     kb = scatter_append(k_buf, k, seqlens_k)
     vb = scatter_append(v_buf, v, seqlens_k)
     out = attention(q, kb, vb, seqlens_k, H, Hkv, scale, local_window_size, attention_bias,
