@@ -20,7 +20,11 @@
  *       max_seq_len; an optional additive attention_bias is added to the
  *       scaled scores;
  *   (4) when the buffer has no room for the new tokens the call fails with
- *       GQA_ERR_KV_OVERFLOW and writes nothing.
+ *       GQA_ERR_KV_OVERFLOW and writes nothing -- unless the caller selects
+ *       the sliding-window cache (dims->kv_eviction = 1; the SWA follow-up of
+ *       the onnxruntime discussion: the op keeps only the
+ *       min(total_sequence_length, cache_capacity) most recent tokens,
+ *       contiguously), in which case the oldest tokens make way.
  *
  * Conventions for every entry point:
  *   - Pointers marked "device" are CUDA device pointers on the current
@@ -74,6 +78,9 @@ typedef struct {
   int32_t bias_heads;         /* 1 or H; ignored when attention_bias is NULL */
   int32_t past_seq_len;       /* Mp: slots of past_key/past_value, 0 <= Mp <= M; read only
                                  when past_key is not present_key (non-shared binding) */
+  int32_t kv_eviction;        /* 0: a full buffer is GQA_ERR_KV_OVERFLOW.  1: sliding-window
+                                 cache of capacity M with contiguous eviction (shared binding
+                                 only; see gqa_forward) */
 } gqa_dims_t;
 
 /*
@@ -81,7 +88,13 @@ typedef struct {
  *
  *   dims             host: problem dimensions (above).
  *   query            device, T [B, S, H*D]   new query rows (heads contiguous per token).
- *   key, value       device, T [B, S, Hkv*D] new key/value rows.
+ *                    Packed QKV (key and value both NULL): T [B, S, (H + 2 Hkv)*D], each
+ *                    token's row holding its H query heads, then its Hkv key heads, then
+ *                    its Hkv value heads, each head D contiguous elements (the
+ *                    [batch, seq, hidden] -> [batch, seq, heads, head_size] reading of
+ *                    "[TorchOnnxToTorch] Add pad+scatter KV cache and mask to GQA").
+ *   key, value       device, T [B, S, Hkv*D] new key/value rows, or both NULL (packed).
+ *                    Only one of them NULL is GQA_ERR_INVALID_ARGUMENT.
  *   past_key         device, T.  Two bindings ("Clarification about GroupQueryAttention
  *   present_key      behavior": the quoted past_key text and ZackyLake's summary):
  *   past_value       - shared: past_key == present_key and past_value == present_value,
@@ -100,9 +113,23 @@ typedef struct {
  *                    Only one of the two pairs equal (or a past buffer equal to the
  *                    other present buffer) returns GQA_ERR_INVALID_ARGUMENT.
  *   seqlens_k        device, int32 [B]: past length P_b of each sequence (0 = empty).
+ *                    With kv_eviction = 1, P_b counts every earlier token of the
+ *                    sequence (the absolute position of its first new token) and may
+ *                    exceed M; the buffer then holds the min(P_b, M) most recent of
+ *                    them at slots [0, min(P_b, M)), slot s holding position
+ *                    P_b - min(P_b, M) + s.  After the call it holds the
+ *                    min(P_b + S, M) most recent tokens the same way (slots beyond keep
+ *                    their bits).  Token i attends over the cached tokens and the new
+ *                    ones (positions P_b - min(P_b, M) ... P_b + i), with the causal
+ *                    mask and window on absolute positions; rotary positions are
+ *                    absolute.  A full buffer is then never an error; P_b < 0 or
+ *                    P_b + S > total_sequence_length stays one (device-recorded
+ *                    GQA_ERR_INVALID_ARGUMENT).  kv_eviction = 1 with the non-shared
+ *                    binding returns GQA_ERR_UNSUPPORTED.
  *   total_sequence_length  host scalar: an upper bound on P_b + S for every b and the
  *                    last dimension of attention_bias.  Must be >= S.  Larger than M:
- *                    GQA_ERR_KV_OVERFLOW before any launch.  A sequence with
+ *                    GQA_ERR_KV_OVERFLOW before any launch (allowed with
+ *                    kv_eviction = 1).  A sequence with
  *                    P_b + S > M (or P_b < 0, or P_b + S > total_sequence_length) is
  *                    detected on the device: that sequence is skipped entirely (no
  *                    slot, no output row written) and the device error word records
@@ -138,8 +165,10 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims,
  * gqa_workspace_size -- bytes of device scratch gqa_forward needs for these
  * dims, total_sequence_length and local_window_size: rotated queries for the
  * generic kernel (head sizes other than 128), key-range partials for a
- * tensor-core prefill grid of fewer than two CTAs per SM, and split-KV
- * partials with their counters for decode.  The figure is for the current
+ * tensor-core prefill grid of fewer than two CTAs per SM, split-KV partials
+ * with their counters for decode, and with kv_eviction = 1 and
+ * total_sequence_length > max_seq_len (a call that may evict) the rotated
+ * queries and new key rows of the evicting path.  The figure is for the current
  * device and covers calls with or without rotary embedding and either
  * binding.  Returns 0 for invalid dims (and when no scratch is needed).
  */
@@ -170,8 +199,9 @@ const char* gqa_status_string(gqa_status_t status);
  * device array of 4 MiB inside the library (held by every GPU that loads it,
  * until exit; a 152-SM GB300 needs at most about 2.5 MB of it); a call that
  * would need more returns GQA_ERR_UNSUPPORTED before any launch, as do shapes
- * other than the decode shape above and the non-shared binding (separate past
- * and present buffers).  The function allocates nothing.
+ * other than the decode shape above, the non-shared binding (separate past
+ * and present buffers), packed QKV and kv_eviction = 1.  The function
+ * allocates nothing.
  *   - All calls on one device share that array and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls whose kernels
  *     can overlap on the GPU race on it: order them on one stream.

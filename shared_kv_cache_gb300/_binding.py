@@ -27,7 +27,7 @@ EXPORTED = ("gqa_forward", "gqa_workspace_size", "gqa_check_device_status", "gqa
 class gqa_dims_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "seq_len", "num_heads", "kv_num_heads", "head_size", "max_seq_len", "dtype",
-        "rotary_interleaved", "cos_cache_rows", "bias_batch", "bias_heads", "past_seq_len")]
+        "rotary_interleaved", "cos_cache_rows", "bias_batch", "bias_heads", "past_seq_len", "kv_eviction")]
 
 
 class GqaError(RuntimeError):
@@ -85,11 +85,12 @@ def _stream(s):
 
 
 def make_dims(batch, seq_len, num_heads, kv_num_heads, head_size, max_seq_len, dtype,
-              rotary_interleaved=0, cos_cache_rows=0, bias_batch=1, bias_heads=1, past_seq_len=0) -> gqa_dims_t:
+              rotary_interleaved=0, cos_cache_rows=0, bias_batch=1, bias_heads=1, past_seq_len=0,
+              kv_eviction=0) -> gqa_dims_t:
     if isinstance(dtype, str):
         dtype = {"fp16": GQA_DTYPE_FP16, "bf16": GQA_DTYPE_BF16}[dtype]
     return gqa_dims_t(batch, seq_len, num_heads, kv_num_heads, head_size, max_seq_len, dtype,
-                      rotary_interleaved, cos_cache_rows, bias_batch, bias_heads, past_seq_len)
+                      rotary_interleaved, cos_cache_rows, bias_batch, bias_heads, past_seq_len, kv_eviction)
 
 
 def gqa_forward(dims, query, key, value, past_key, past_value, present_key, present_value, seqlens_k,

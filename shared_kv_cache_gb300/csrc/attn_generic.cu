@@ -8,6 +8,12 @@
 // token's own position p = past_b + i and stops there ("KV Cache", "Short
 // summary of notes": early exit at the current length instead of sweeping
 // max_seq_len).  Online softmax in fp32.
+//
+// Evicting sliding-window cache (a call that may evict): the buffer holds
+// the min(P_b, M) most recent earlier tokens from slot 0, and the new tokens
+// are not in it yet, so keys at positions below P_b are read from slot
+// (position - P_b + min(P_b, M)) and the others from the step's rotated new
+// key rows and input value rows.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,6 +31,13 @@ struct GenericParams {
   int B, S, H, Hkv, D, M, total, window;
   int bias_b, bias_h;
   float scale_log2;
+  int q_stride;  // elements between consecutive tokens' query rows
+  // evicting call: new key rows (rotated) [B, S, Hkv, D] and the input value
+  // rows (kv_stride elements apart); nullptr otherwise
+  const void* k_new;
+  const void* v_new;
+  int kv_stride;
+  int evict;  // sliding-window cache: a full buffer is not an error
 };
 
 constexpr int kWarps = 4;
@@ -39,13 +52,15 @@ __global__ void __launch_bounds__(kWarps * 32) attn_generic_kernel(GenericParams
   const int i = (int)((row / p.H) % p.S);
   const int b = (int)(row / ((long long)p.H * p.S));
   const int past = p.seqlens[b];
-  if (sequence_error(past, p.S, p.M, p.total)) return;  // recorded by the append kernel
+  if (sequence_error(past, p.S, p.M, p.total, p.evict)) return;  // recorded by the append kernel
   const int G = p.H / p.Hkv;
   const int kh = h / G;
   const int pos = past + i;
-  const int lo = p.window > 0 ? max(0, pos - p.window + 1) : 0;
+  // slot s of the buffer holds position s + first (first = 0 unless evicting)
+  const int first = p.k_new ? slot0_position(past, p.M) : 0;
+  const int lo = max(first, p.window > 0 ? max(0, pos - p.window + 1) : 0);
 
-  const T* qrow = static_cast<const T*>(p.q) + (((size_t)b * p.S + i) * p.H + h) * p.D;
+  const T* qrow = static_cast<const T*>(p.q) + ((size_t)b * p.S + i) * p.q_stride + (size_t)h * p.D;
   const T* kb = static_cast<const T*>(p.kbuf) + ((size_t)b * p.Hkv + kh) * p.M * p.D;
   const T* vb = static_cast<const T*>(p.vbuf) + ((size_t)b * p.Hkv + kh) * p.M * p.D;
   const T* brow = nullptr;
@@ -63,7 +78,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_generic_kernel(GenericParams
   }
   float m = -INFINITY, l = 0.f;
   for (int j = lo; j <= pos; ++j) {
-    const T* kr = kb + (size_t)j * p.D;
+    const bool fresh = p.k_new && j >= past;  // a new token, not yet in the buffer
+    const T* kr = fresh ? static_cast<const T*>(p.k_new) + (((size_t)b * p.S + (j - past)) * p.Hkv + kh) * p.D
+                        : kb + (size_t)(j - first) * p.D;
     float s = 0.f;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -79,7 +96,9 @@ __global__ void __launch_bounds__(kWarps * 32) attn_generic_kernel(GenericParams
     const float corr = fast_exp2(m - mu);
     const float pj = fast_exp2(s - mu);
     l = l * corr + pj;
-    const T* vr = vb + (size_t)j * p.D;
+    const T* vr = fresh ? static_cast<const T*>(p.v_new) + ((size_t)b * p.S + (j - past)) * p.kv_stride +
+                              (size_t)kh * p.D
+                        : vb + (size_t)(j - first) * p.D;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int d = lane + 32 * t;
@@ -97,9 +116,11 @@ __global__ void __launch_bounds__(kWarps * 32) attn_generic_kernel(GenericParams
 }
 
 template <typename T>
-cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
+cudaError_t launch_t(const ForwardArgs& a, const void* q_src, const void* k_new) {
+  // the rotated queries in the workspace are [B, S, H, D]; raw ones keep the input's row stride
   GenericParams p{q_src, a.kbuf, a.vbuf, a.seqlens, a.bias, a.out, a.err, a.B, a.S, a.H, a.Hkv, a.D,
-                  a.M, a.total, a.window, a.bias_b, a.bias_h, a.scale * kLog2e};
+                  a.M, a.total, a.window, a.bias_b, a.bias_h, a.scale * kLog2e,
+                  q_src == a.q ? a.q_stride : a.H * a.D, k_new, k_new ? a.v : nullptr, a.kv_stride, a.evict};
   const long long rows = (long long)a.B * a.S * a.H;
   const dim3 grid((unsigned)((rows + kWarps - 1) / kWarps));
   const int nt = (a.D + 31) / 32;
@@ -118,8 +139,8 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
 
 }  // namespace
 
-cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src) {
-  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src) : launch_t<__half>(a, q_src);
+cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src, const void* k_new) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src, k_new) : launch_t<__half>(a, q_src, k_new);
 }
 
 }  // namespace gqa

@@ -72,13 +72,19 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 }
 
 // Checks a sequence's lengths the same way the host documents it.  Returns 0
-// when the sequence may be processed, else the error code it raises.
-__device__ __forceinline__ int sequence_error(int past, int S, int M, int total) {
+// when the sequence may be processed, else the error code it raises.  With
+// the evicting sliding-window cache (`evict`) a full buffer is not an error.
+__device__ __forceinline__ int sequence_error(int past, int S, int M, int total, int evict = 0) {
   if (past < 0) return GQA_ERR_INVALID_ARGUMENT;
-  if ((long long)past + S > M) return GQA_ERR_KV_OVERFLOW;
+  if (!evict && (long long)past + S > M) return GQA_ERR_KV_OVERFLOW;
   if ((long long)past + S > total) return GQA_ERR_INVALID_ARGUMENT;
   return 0;
 }
+
+// Evicting cache: the tokens of a sequence with P tokens before the call that
+// the buffer holds on entry (min(P, M)), and the absolute position of slot 0.
+__device__ __forceinline__ int cached_tokens(int past, int M) { return past < M ? past : M; }
+__device__ __forceinline__ int slot0_position(int past, int M) { return past - cached_tokens(past, M); }
 
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers, bulk copies

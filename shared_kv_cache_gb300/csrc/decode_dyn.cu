@@ -39,6 +39,11 @@
 // KV cache and mask to GQA", PR description: rotary at arange + past length,
 // scatter at seqlens_k) and patches that row into the shared-memory tile, so
 // the TMA load never has to observe the global write.
+//
+// Evicting sliding-window cache (a call that may evict): slot s of an item
+// holds key position s + slot0_position(P_b, M), the tiles are addressed in
+// slots, and the new row is only patched into shared memory: the buffer is
+// rewritten afterwards by the eviction kernel, once every read is done.
 #include "common.cuh"
 #include "internal.h"
 
@@ -127,6 +132,9 @@ struct DynParams {
   unsigned long long* arrivals;  // [slots] per-item arrival counters (epoch, count), at the item's first slot
   int* err;
   int B, H, Hkv, G, M, total, window, P, interleaved, bias_b, bias_h, chunks_per_cta;
+  int q_stride, kv_stride;  // elements between consecutive sequences' query / key and value rows
+  int evict;                // sliding-window cache: a full buffer is not an error
+  int evicting;             // keys addressed through the cache's slot base; no append here
   uint32_t epoch;
   float scale_log2;
 };
@@ -140,12 +148,13 @@ __device__ __forceinline__ uint32_t sw_off(int r, int c) {
 // Keys of sequence b: [lo, L); returns its tile count (0 when the sequence
 // fails the length check and is skipped).
 __device__ __forceinline__ int seq_tiles(const DynParams& p, int past, int& lo, int& L) {
-  if (sequence_error(past, 1, p.M, p.total)) {
+  if (sequence_error(past, 1, p.M, p.total, p.evict)) {
     lo = L = 0;
     return 0;
   }
   L = past + 1;
   lo = p.window > 0 ? max(0, L - p.window) : 0;
+  if (p.evicting) lo = max(lo, slot0_position(past, p.M));  // older keys have left the cache
   return (L - lo + kTile - 1) / kTile;
 }
 
@@ -345,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int* sl = cached ? s_seq : p.seqlens;
     if (c == 0)  // sequences that fail the length check are skipped and reported once
       for (int i = lane; i < p.B; i += 32) {
-        const int e = sequence_error(sl[i], 1, p.M, p.total);
+        const int e = sequence_error(sl[i], 1, p.M, p.total, p.evict);
         if (e) record_error(p.err, e);
       }
     Partition pt;
@@ -363,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     bool ok = true;
     // (lane 0) K/V tiles [ta, tb_) of chunk d into the ring
     auto issue_tiles = [&](const ChunkDesc& d, int ta, int tb_) {
-      const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo;
+      const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo - (p.evicting ? slot0_position(d.L - 1, p.M) : 0);
       for (int t = ta; t < tb_ && ok; ++t, ++gt) {
         const int st = gt % kStages;
         const int round = gt / kStages;
@@ -407,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t bytes = G * kD * 2 + (rot ? 256u : 0u) + (has_new ? 512u : 0u);
           const uint32_t fb = bar_dfull + 8 * ds;
           mbar_arrive_expect_tx(fb, bytes);
-          bulk_g2s(slot + st_q(), static_cast<const T*>(p.q) + ((size_t)d.b * p.H + (size_t)d.kh * G) * kD,
+          bulk_g2s(slot + st_q(), static_cast<const T*>(p.q) + (size_t)d.b * p.q_stride + (size_t)d.kh * G * kD,
                    G * kD * 2, fb);
           if (rot) {
             const size_t crow = (size_t)(d.L - 1) * (kD / 2);
@@ -415,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             bulk_g2s(slot + st_sin(G), static_cast<const T*>(p.sin) + crow, 128, fb);
           }
           if (has_new) {
-            const size_t row = ((size_t)d.b * p.Hkv + d.kh) * kD;
+            const size_t row = (size_t)d.b * p.kv_stride + (size_t)d.kh * kD;
             bulk_g2s(slot + st_kn(G), static_cast<const T*>(p.knew) + row, 256, fb);
             bulk_g2s(slot + st_vn(G), static_cast<const T*>(p.vnew) + row, 256, fb);
           }
@@ -673,12 +682,12 @@ __global__ void __launch_bounds__(kThreads, 2)
           V8 k1, k2;
           rotate8(st_k, k1, k2);
           store8(news, k1, k2);
-          store8(static_cast<T*>(p.kbuf) + row, k1, k2);
+          if (!p.evicting) store8(static_cast<T*>(p.kbuf) + row, k1, k2);
         } else if (tid < 24) {
           const int dd = (tid - 8) * 8;
           const V8 vv = *reinterpret_cast<const V8*>(st_v + dd);
           *reinterpret_cast<V8*>(news + kD + dd) = vv;
-          *reinterpret_cast<V8*>(static_cast<T*>(p.vbuf) + row + dd) = vv;
+          if (!p.evicting) *reinterpret_cast<V8*>(static_cast<T*>(p.vbuf) + row + dd) = vv;
         }
       }
     }
@@ -1008,6 +1017,10 @@ cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, uint8_t* ws, uint32
   p.bias_b = a.bias_b;
   p.bias_h = a.bias_h;
   p.chunks_per_cta = kDecodeChunksPerCta;
+  p.q_stride = a.q_stride;
+  p.kv_stride = a.kv_stride;
+  p.evict = a.evict;
+  p.evicting = a.evicting;
   p.epoch = epoch;
   p.scale_log2 = a.scale * kLog2e;
   const int smem = layout_for(G).total;

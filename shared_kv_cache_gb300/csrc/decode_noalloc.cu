@@ -96,7 +96,8 @@ extern "C" gqa_status_t gqa_decode_noalloc(const gqa_dims_t* dims, const void* q
   // only the split-KV decode kernels have this variant
   if (S != 1 || D != 128 || H / Hkv > kDecodeMaxGroup) return GQA_ERR_UNSUPPORTED;
   if ((long long)B * Hkv * M >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
-  if (!key && !value) return GQA_ERR_UNSUPPORTED;
+  if (!key && !value) return GQA_ERR_UNSUPPORTED;  // packed QKV: not taken here
+  if (dims->kv_eviction != 0) return GQA_ERR_UNSUPPORTED;  // the evicting cache: not taken here
   if (!query || !key || !value || !past_key || !past_value || !present_key || !present_value || !seqlens_k ||
       !output)
     return GQA_ERR_INVALID_ARGUMENT;
@@ -134,6 +135,8 @@ extern "C" gqa_status_t gqa_decode_noalloc(const gqa_dims_t* dims, const void* q
   a.window = local_window_size > 0 ? local_window_size : 0;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.q = query; a.k = key; a.v = value;
+  a.q_stride = H * D;
+  a.kv_stride = Hkv * D;
   a.kbuf = present_key; a.vbuf = present_value;
   a.seqlens = seqlens_k;
   a.cos = cos_cache; a.sin = sin_cache;

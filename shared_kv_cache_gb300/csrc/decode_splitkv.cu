@@ -90,6 +90,7 @@ struct DecodeParams {
   int* err;
   int B, H, Hkv, G, M, total, window, P, interleaved, bias_b, bias_h;
   float scale_log2;
+  int q_stride, kv_stride;  // elements between consecutive sequences' query / key and value rows
 };
 
 // Byte offset of 16-byte chunk c (0..15) of row r inside a [kTile x 128]
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // 16-byte asynchronous copies, so that their latency hides behind the
   // previous segment's tiles.
   auto prefetch = [&](int pb, int pkh, int ppast, bool pnew) {
-    const T* qg = static_cast<const T*>(p.q) + ((size_t)pb * p.H + (size_t)pkh * G) * kD;
+    const T* qg = static_cast<const T*>(p.q) + (size_t)pb * p.q_stride + (size_t)pkh * G * kD;
     for (int u = tid; u < G * 16; u += kCW * 32) cp_async16(st_q + u * 8, qg + u * 8);
     if (rot && tid < 16) {
       const T* src = static_cast<const T*>(tid < 8 ? p.cos : p.sin) + (size_t)ppast * (kD / 2) + (tid & 7) * 8;
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (pnew && tid >= 32 && tid < 64) {
       const int u = tid - 32;
-      const size_t row = ((size_t)pb * p.Hkv + pkh) * kD;
+      const size_t row = (size_t)pb * p.kv_stride + (size_t)pkh * kD;
       if (u < 16)
         cp_async16(st_kn + u * 8, static_cast<const T*>(p.knew) + row + u * 8);
       else
@@ -811,7 +812,7 @@ cudaError_t launch_t(const ForwardArgs& a, const Plan& plan, float* part_o, floa
   const int G = a.H / a.Hkv;
   DecodeParams p{a.q, a.k, a.v, a.kbuf, a.vbuf, a.seqlens, a.cos, a.sin, a.bias, a.out, part_o, part_ml, a.err,
                  a.B, a.H, a.Hkv, G, a.M, a.total, a.window, plan.ctas, a.interleaved, a.bias_b, a.bias_h,
-                 a.scale * kLog2e};
+                 a.scale * kLog2e, a.q_stride, a.kv_stride};
   const int smem = layout_for(G).total;
   auto kern = G <= 8 ? decode_kernel<T, 1> : decode_kernel<T, 2>;
   static std::atomic<int> smem_set[2][kMaxDevices];  // limit set so far, per variant and device

@@ -76,6 +76,7 @@ gqa_status_t check_dims(const gqa_dims_t* d) {
   if (d->head_size < 8 || d->head_size > 256 || d->head_size % 8 != 0) return GQA_ERR_INVALID_ARGUMENT;
   if (d->dtype != GQA_DTYPE_FP16 && d->dtype != GQA_DTYPE_BF16) return GQA_ERR_INVALID_ARGUMENT;
   if (d->rotary_interleaved != 0 && d->rotary_interleaved != 1) return GQA_ERR_INVALID_ARGUMENT;
+  if (d->kv_eviction != 0 && d->kv_eviction != 1) return GQA_ERR_INVALID_ARGUMENT;
   // every index the kernels form stays within 32-bit row counts / 64-bit bytes
   const long long rows = (long long)d->batch * d->kv_num_heads * d->max_seq_len;
   if (rows >= (1ll << 31)) return GQA_ERR_UNSUPPORTED;
@@ -116,7 +117,8 @@ int* device_error_word() { return error_word_ptr(); }
 int device_sm_count() { return sm_count(); }
 int device_smem_per_sm() { return smem_per_sm(); }
 
-Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms) {
+Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms,
+               bool evicting) {
   Plan pl{};
   const int G = H / Hkv;
   if (S == 1 && D == 128 && G <= kDecodeMaxGroup) {
@@ -140,6 +142,18 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
     pl.total_bytes = off;
     (void)total;
     (void)window;
+    return pl;
+  }
+  // a call that may evict attends over the cached tokens and the new rows
+  // (not yet in the buffer) on CUDA cores: rotated queries and keys go to
+  // the workspace
+  if (evicting) {
+    pl.path = Path::kGeneric;
+    pl.q_rot_off = 0;
+    pl.q_rot_bytes = rotary ? (size_t)B * S * H * D * 2 : 0;
+    pl.k_new_off = align_up(pl.q_rot_bytes, 256);
+    pl.k_new_bytes = (size_t)B * S * Hkv * D * 2;
+    pl.total_bytes = align_up(pl.k_new_off + pl.k_new_bytes, 256);
     return pl;
   }
   pl.path = (S > 1 && D == 128) ? Path::kPrefillTC : Path::kGeneric;
@@ -246,8 +260,9 @@ const char* gqa_status_string(gqa_status_t s) {
 
 size_t gqa_workspace_size(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size) {
   if (check_dims(dims) != GQA_OK || total_sequence_length < dims->seq_len) return 0;
+  const bool evicting = dims->kv_eviction == 1 && total_sequence_length > dims->max_seq_len;
   const Plan pl = make_plan(dims->batch, dims->seq_len, dims->num_heads, dims->kv_num_heads, dims->head_size,
-                            total_sequence_length, local_window_size, true, sm_count());
+                            total_sequence_length, local_window_size, true, sm_count(), evicting);
   return pl.total_bytes;
 }
 
@@ -271,8 +286,13 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   const int B = dims->batch, S = dims->seq_len, H = dims->num_heads, Hkv = dims->kv_num_heads;
   const int D = dims->head_size, M = dims->max_seq_len;
 
-  // packed QKV (key and value absent) is a form this library does not take
-  if (!key && !value) return GQA_ERR_UNSUPPORTED;
+  // packed QKV: key and value absent, query [B, S, (H + 2 Hkv) * D] holding
+  // each token's query heads, then its key heads, then its value heads
+  const bool packed = !key && !value;
+  if (packed && query) {
+    key = static_cast<const uint8_t*>(query) + (size_t)H * D * 2;
+    value = static_cast<const uint8_t*>(query) + (size_t)(H + Hkv) * D * 2;
+  }
   if (!query || !key || !value || !past_key || !past_value || !present_key || !present_value || !seqlens_k ||
       !output)
     return GQA_ERR_INVALID_ARGUMENT;
@@ -280,6 +300,8 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   // (four distinct buffers; the present becomes past + new)
   const bool shared = past_key == present_key && past_value == present_value;
   if (present_key == present_value) return GQA_ERR_INVALID_ARGUMENT;
+  const bool evict = dims->kv_eviction == 1;
+  if (evict && !shared) return GQA_ERR_UNSUPPORTED;  // the evicting cache is one shared buffer
   if (!shared) {
     if (past_key == present_key || past_value == present_value || past_key == past_value ||
         past_key == present_value || past_value == present_key)
@@ -291,7 +313,9 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
       misaligned(present_value) || misaligned(output) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
     return GQA_ERR_INVALID_ARGUMENT;
   if (total_sequence_length < S) return GQA_ERR_INVALID_ARGUMENT;
-  if (total_sequence_length > M) return GQA_ERR_KV_OVERFLOW;
+  if (total_sequence_length > M && !evict) return GQA_ERR_KV_OVERFLOW;
+  // a call that may evict (some P_b + S may exceed M; the host cannot tell which)
+  const bool evicting = evict && total_sequence_length > M;
   if ((cos_cache == nullptr) != (sin_cache == nullptr)) return GQA_ERR_INVALID_ARGUMENT;
   if (cos_cache) {
     if (misaligned(cos_cache) || misaligned(sin_cache)) return GQA_ERR_INVALID_ARGUMENT;
@@ -305,7 +329,8 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   if (!(std::isfinite(scale))) return GQA_ERR_INVALID_ARGUMENT;
 
   const int nsm = sm_count();
-  const Plan pl = make_plan(B, S, H, Hkv, D, total_sequence_length, local_window_size, cos_cache != nullptr, nsm);
+  const Plan pl =
+      make_plan(B, S, H, Hkv, D, total_sequence_length, local_window_size, cos_cache != nullptr, nsm, evicting);
   if (workspace_bytes < pl.total_bytes || (pl.total_bytes > 0 && !workspace)) return GQA_ERR_INVALID_ARGUMENT;
   if (pl.total_bytes > 0 && misaligned(workspace)) return GQA_ERR_INVALID_ARGUMENT;
 
@@ -318,8 +343,12 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
   a.interleaved = dims->rotary_interleaved;
   a.total = total_sequence_length;
   a.window = local_window_size > 0 ? local_window_size : 0;
+  a.evict = evict ? 1 : 0;
+  a.evicting = evicting ? 1 : 0;
   a.scale = scale > 0.f ? scale : 1.0f / std::sqrt((float)D);
   a.q = query; a.k = key; a.v = value;
+  a.q_stride = packed ? (H + 2 * Hkv) * D : H * D;
+  a.kv_stride = packed ? (H + 2 * Hkv) * D : Hkv * D;
   a.kbuf = present_key; a.vbuf = present_value;
   a.seqlens = seqlens_k;
   a.cos = cos_cache; a.sin = sin_cache;
@@ -346,15 +375,19 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
     case Path::kPrefillTC:
     case Path::kGeneric: {
       void* q_rot = (cos_cache && pl.path == Path::kGeneric) ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
-      e = launch_rope_append(a, q_rot);
+      void* k_new = evicting ? static_cast<void*>(ws + pl.k_new_off) : nullptr;
+      e = launch_rope_append(a, q_rot, k_new);
       if (e == cudaSuccess)
         e = pl.path == Path::kPrefillTC
                 ? launch_prefill_tc(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
                                     reinterpret_cast<float*>(ws + pl.part_ml_off))
-                : launch_attn_generic(a, q_rot ? q_rot : query);
+                : launch_attn_generic(a, q_rot ? q_rot : query, k_new);
       break;
     }
   }
+  // the evicting cache: once attention has read the buffer, keep the most
+  // recent tokens contiguously and write the new rows
+  if (e == cudaSuccess && evicting) e = launch_evict_shift(a);
   if (e == cudaSuccess && stage_out) e = launch_stage(*stage_out, a.stream, nsm);
   return e == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -371,17 +404,19 @@ void* mapped_host(const void* p) {
 }
 
 // gqa_forward_host's workspace: gqa_forward's scratch, then the device copies
-// of the step's inputs and output, each 256-byte aligned.
+// of the step's inputs and output, each 256-byte aligned.  With packed QKV
+// the query copy holds all three and the key/value copies are empty.
 struct HostStaging {
   size_t q, k, v, s, o, total;
-  size_t qb, kb, sb;  // bytes of query (= output), key (= value), seqlens_k
-  size_t base;        // gqa_forward's part
+  size_t qb, kb, sb, ob;  // bytes of query, key (= value), seqlens_k, output
+  size_t base;            // gqa_forward's part
 };
-HostStaging host_staging(const gqa_dims_t* d, int32_t total, int32_t window) {
+HostStaging host_staging(const gqa_dims_t* d, int32_t total, int32_t window, bool packed) {
   HostStaging h{};
   const size_t rows = (size_t)d->batch * d->seq_len;
-  h.qb = rows * d->num_heads * d->head_size * 2;
-  h.kb = rows * d->kv_num_heads * d->head_size * 2;
+  h.ob = rows * d->num_heads * d->head_size * 2;
+  h.qb = packed ? rows * (d->num_heads + 2 * d->kv_num_heads) * d->head_size * 2 : h.ob;
+  h.kb = packed ? 0 : rows * d->kv_num_heads * d->head_size * 2;
   h.sb = (size_t)d->batch * 4;
   h.base = align_up(gqa_workspace_size(d, total, window), 256);
   h.q = h.base;
@@ -389,7 +424,7 @@ HostStaging host_staging(const gqa_dims_t* d, int32_t total, int32_t window) {
   h.v = h.k + align_up(h.kb, 256);
   h.s = h.v + align_up(h.kb, 256);
   h.o = h.s + align_up(h.sb, 256);
-  h.total = h.o + align_up(h.qb, 256);
+  h.total = h.o + align_up(h.ob, 256);
   return h;
 }
 
@@ -410,7 +445,9 @@ gqa_status_t gqa_forward(const gqa_dims_t* dims, const void* query, const void* 
 
 size_t gqa_workspace_size_host(const gqa_dims_t* dims, int32_t total_sequence_length, int32_t local_window_size) {
   if (check_dims(dims) != GQA_OK || total_sequence_length < dims->seq_len) return 0;
-  return host_staging(dims, total_sequence_length, local_window_size).total;
+  // enough for either input form (separate or packed QKV)
+  return std::max(host_staging(dims, total_sequence_length, local_window_size, false).total,
+                  host_staging(dims, total_sequence_length, local_window_size, true).total);
 }
 
 gqa_status_t gqa_forward_host(const gqa_dims_t* dims, const void* query, const void* key, const void* value,
@@ -421,31 +458,32 @@ gqa_status_t gqa_forward_host(const gqa_dims_t* dims, const void* query, const v
                               void* workspace, size_t workspace_bytes, void* stream) {
   gqa_status_t st = check_dims(dims);
   if (st != GQA_OK) return st;
-  if (!key && !value) return GQA_ERR_UNSUPPORTED;
-  if (!query || !key || !value || !seqlens_k || !output) return GQA_ERR_INVALID_ARGUMENT;
+  const bool packed = !key && !value;  // query holds the key and value rows too
+  if (!query || (!packed && (!key || !value)) || !seqlens_k || !output) return GQA_ERR_INVALID_ARGUMENT;
   if (misaligned(query) || misaligned(key) || misaligned(value) || misaligned(output) ||
       (reinterpret_cast<uintptr_t>(seqlens_k) & 3u))
     return GQA_ERR_INVALID_ARGUMENT;
   if (total_sequence_length < dims->seq_len) return GQA_ERR_INVALID_ARGUMENT;
-  const HostStaging h = host_staging(dims, total_sequence_length, local_window_size);
+  const HostStaging h = host_staging(dims, total_sequence_length, local_window_size, packed);
   if (!workspace || workspace_bytes < h.total || misaligned(workspace)) return GQA_ERR_INVALID_ARGUMENT;
   void* dq = mapped_host(query);
-  void* dk = mapped_host(key);
-  void* dv = mapped_host(value);
+  void* dk = packed ? nullptr : mapped_host(key);
+  void* dv = packed ? nullptr : mapped_host(value);
   void* ds = mapped_host(seqlens_k);
   void* dout = mapped_host(output);
-  if (!dq || !dk || !dv || !ds || !dout) return GQA_ERR_INVALID_ARGUMENT;
+  if (!dq || (!packed && (!dk || !dv)) || !ds || !dout) return GQA_ERR_INVALID_ARGUMENT;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   StageList in;
-  in.seg[0] = StageSeg{dq, ws + h.q, h.qb};
-  in.seg[1] = StageSeg{dk, ws + h.k, h.kb};
-  in.seg[2] = StageSeg{dv, ws + h.v, h.kb};
-  in.seg[3] = StageSeg{ds, ws + h.s, h.sb};
-  in.n = 4;
+  in.seg[in.n++] = StageSeg{dq, ws + h.q, h.qb};
+  if (!packed) {
+    in.seg[in.n++] = StageSeg{dk, ws + h.k, h.kb};
+    in.seg[in.n++] = StageSeg{dv, ws + h.v, h.kb};
+  }
+  in.seg[in.n++] = StageSeg{ds, ws + h.s, h.sb};
   StageList out;
-  out.seg[0] = StageSeg{ws + h.o, dout, h.qb};
+  out.seg[0] = StageSeg{ws + h.o, dout, h.ob};
   out.n = 1;
-  return forward_impl(dims, ws + h.q, ws + h.k, ws + h.v, past_key, past_value, present_key, present_value,
+  return forward_impl(dims, ws + h.q, packed ? nullptr : ws + h.k, packed ? nullptr : ws + h.v, past_key, past_value, present_key, present_value,
                       reinterpret_cast<const int32_t*>(ws + h.s), total_sequence_length, cos_cache, sin_cache,
                       scale, local_window_size, attention_bias, ws + h.o, workspace, h.base, stream, &in, &out,
                       dout);

@@ -19,10 +19,14 @@ struct ForwardArgs {
   int interleaved;  // rotary pairing
   int total;        // total_sequence_length
   int window;       // <= 0: none
+  int evict;        // sliding-window cache with contiguous eviction (dims->kv_eviction)
+  int evicting;     // this call may evict (evict and total > M): the buffer is rewritten after attention
   float scale;      // resolved (> 0)
   const void* q;
   const void* k;
   const void* v;
+  int q_stride;   // elements from one token's query row to the next: H*D, or (H + 2 Hkv)*D packed
+  int kv_stride;  // the same for the key and value rows: Hkv*D, or (H + 2 Hkv)*D packed
   void* kbuf;
   void* vbuf;
   const int32_t* seqlens;
@@ -38,12 +42,18 @@ struct ForwardArgs {
 
 enum class Path { kDecode, kPrefillTC, kGeneric };
 
+// With `evicting` set (ForwardArgs::evicting), the decode and generic
+// kernels attend over the cached and the new tokens without writing the
+// buffer, and launch_evict_shift then moves each (sequence, KV head)'s kept
+// tokens to slots [0, n_keep) and writes the new rows.
+
 // Which kernels run and how the workspace is carved up.  Derived from the
 // dims alone, so gqa_workspace_size() and gqa_forward() agree.
 struct Plan {
   Path path;
   int ctas = 0;    // decode: persistent grid size P
   size_t q_rot_off = 0, q_rot_bytes = 0;    // rotated queries, T [B, S, H, D]
+  size_t k_new_off = 0, k_new_bytes = 0;    // evicting generic path: rotated new keys, T [B, S, Hkv, D]
   size_t part_o_off = 0, part_o_bytes = 0;  // decode partial outputs, f32 [slots, G, D]; prefill splits f32 [rows, D]
   size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [slots, G, 2]
   size_t sched_off = 0, sched_bytes = 0;      // decode chunk ticket + per-item arrival counters, u64 [1 + slots]
@@ -52,7 +62,8 @@ struct Plan {
   size_t total_bytes = 0;
 };
 
-Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms);
+Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms,
+               bool evicting = false);
 
 // The current device's error word (device address), SM count and shared
 // memory per SM.
@@ -61,11 +72,20 @@ int device_sm_count();
 int device_smem_per_sm();
 
 // Kernel launchers (each returns the launch's cudaError_t).
-cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot);
+// Rotary + append; with k_new set (evicting path) the rotated key rows go to
+// k_new [B, S, Hkv, D] instead of the buffer and the value rows are not
+// copied.
+cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new = nullptr);
+// Evicting cache: keep the min(P_b + S, M) most recent tokens of every
+// (sequence, KV head) at slots [0, n_keep), new rows included (after the
+// step's attention has read the buffer).
+cudaError_t launch_evict_shift(const ForwardArgs& a);
 // Non-shared binding: slots [0, past_b) of the present buffers (a.kbuf,
 // a.vbuf) copied from past buffers of Mp slots.
 cudaError_t launch_present_copy(const ForwardArgs& a, const void* past_k, const void* past_v, int Mp);
-cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src);
+// With a.evicting, keys at positions >= P_b come from k_new [B, S, Hkv, D]
+// and the input value rows.
+cudaError_t launch_attn_generic(const ForwardArgs& a, const void* q_src, const void* k_new = nullptr);
 // Split-KV decode with a static partition and a separate combine kernel
 // (partials f32 [P, 2, G, D] and [P, 2, G, 2]; used by gqa_decode_noalloc).
 cudaError_t launch_decode(const ForwardArgs& a, const Plan& plan, float* part_o, float* part_ml);

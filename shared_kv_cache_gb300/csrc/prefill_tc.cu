@@ -79,6 +79,7 @@ struct PrefillParams {
   int B, S, H, Hkv, G, M, total, window, bias_b, bias_h, n_qt, n_pairs, interleaved;
   int n_split;     // key-range splits per work item (1: none)
   float scale_log2;
+  int evict;       // sliding-window cache: a full buffer is not an error (no call here evicts)
 };
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hA = kh * p.G + 2 * pr;
   const bool has_b = 2 * pr + 1 < p.G;
   const int past = p.seqlens[b];
-  if (sequence_error(past, p.S, p.M, p.total)) return;  // recorded by the append kernel
+  if (sequence_error(past, p.S, p.M, p.total, p.evict)) return;  // recorded by the append kernel
   const int i0 = qt * kBM;
   const int i1 = min(i0 + kBM, p.S);
   const int L = past + p.S;
@@ -616,7 +617,7 @@ __global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParam
   const int b = valid ? (int)(r / ((long long)p.H * p.S)) : 0;
   const int past = valid ? p.seqlens[b] : 0;
   pdl_wait_primary();
-  if (!valid || sequence_error(past, p.S, p.M, p.total)) return;
+  if (!valid || sequence_error(past, p.S, p.M, p.total, p.evict)) return;
   const int qt = i / kBM, i0 = qt * kBM, i1 = min(i0 + kBM, p.S);
   const int kstart = p.window > 0 ? max(0, past + i0 - p.window + 1) : 0;
   const int n_all = (past + i1 - kstart + kBN - 1) / kBN;
@@ -657,7 +658,8 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   CUtensorMap qmap, kmap, vmap;
   {
     const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.S, (cuuint64_t)a.B};
-    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2, (cuuint64_t)a.S * a.H * kD * 2};
+    // token rows a.q_stride elements apart (H * D, or (H + 2 Hkv) * D packed)
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.q_stride * 2, (cuuint64_t)a.S * a.q_stride * 2};
     const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
     if (!encode_tensor_map(&qmap, dt, 4, const_cast<void*>(q_src), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
@@ -697,6 +699,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   p.interleaved = a.interleaved;
   p.n_split = n_split;
   p.scale_log2 = a.scale * kLog2e;
+  p.evict = a.evict;
   auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
   static std::atomic<int> smem_set[2][kMaxDevices];  // limit set so far, per instantiation and device
   {

@@ -28,6 +28,9 @@ struct RopeParams {
   const void* sin;
   int* err;
   int S, H, Hkv, D, M, total, interleaved;
+  int q_stride, kv_stride;  // elements between consecutive tokens' query / key and value rows
+  void* k_new;              // evicting path: rotated key rows go here, [B, S, Hkv, D]; nullptr: to the buffer
+  int evict;                // sliding-window cache: a full buffer is not an error
 };
 
 template <typename T, int VEC>
@@ -77,7 +80,7 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
   const int b = tok / p.S;
   const int i = tok - b * p.S;
   const int past = p.seqlens[b];
-  const int e = sequence_error(past, p.S, p.M, p.total);
+  const int e = sequence_error(past, p.S, p.M, p.total, p.evict);
   if (e) {
     if (i == 0 && threadIdx.x == 0) record_error(p.err, e);
     return;
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
   const bool rot = p.cos != nullptr;
   const int nq = (rot && p.q_rot) ? p.H * npv : 0;
   const int nk = p.Hkv * npv;
-  const int nvu = p.Hkv * (D / (2 * VEC));   // value copy units of 2*VEC elements
+  const int nvu = p.k_new ? 0 : p.Hkv * (D / (2 * VEC));   // value copy units of 2*VEC elements
   const T* q = static_cast<const T*>(p.q);
   const T* k = static_cast<const T*>(p.k);
   const T* v = static_cast<const T*>(p.v);
@@ -104,8 +107,11 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
       const int uu = isq ? u : u - nq;
       const int head = uu / npv;
       const int jv = (uu - head * npv) * VEC;
-      const T* src = isq ? q + ((size_t)tok * p.H + head) * D : k + ((size_t)tok * p.Hkv + head) * D;
-      T* dst = isq ? qr + ((size_t)tok * p.H + head) * D : kb + (((size_t)b * p.Hkv + head) * p.M + pos) * D;
+      const T* src = isq ? q + (size_t)tok * p.q_stride + (size_t)head * D
+                         : k + (size_t)tok * p.kv_stride + (size_t)head * D;
+      T* dst = isq      ? qr + ((size_t)tok * p.H + head) * D
+               : p.k_new ? static_cast<T*>(p.k_new) + ((size_t)tok * p.Hkv + head) * D
+                         : kb + (((size_t)b * p.Hkv + head) * p.M + pos) * D;
       if (rot) {
         rotate_vec<T, VEC>(src, dst, cosr, sinr, jv, half, p.interleaved != 0);
       } else {
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
       const int per = D / (2 * VEC);
       const int head = uu / per;
       const int off = (uu - head * per) * 2 * VEC;
-      const T* src = v + ((size_t)tok * p.Hkv + head) * D + off;
+      const T* src = v + (size_t)tok * p.kv_stride + (size_t)head * D + off;
       T* dst = vb + (((size_t)b * p.Hkv + head) * p.M + pos) * D + off;
       *reinterpret_cast<V*>(dst) = *reinterpret_cast<const V*>(src);
       *reinterpret_cast<V*>(dst + VEC) = *reinterpret_cast<const V*>(src + VEC);
@@ -127,9 +133,9 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
 }
 
 template <typename T>
-cudaError_t launch_t(const ForwardArgs& a, void* q_rot) {
+cudaError_t launch_t(const ForwardArgs& a, void* q_rot, void* k_new) {
   RopeParams p{a.q, a.k, a.v, q_rot, a.kbuf, a.vbuf, a.seqlens, a.cos, a.sin, a.err,
-               a.S, a.H, a.Hkv, a.D, a.M, a.total, a.interleaved};
+               a.S, a.H, a.Hkv, a.D, a.M, a.total, a.interleaved, a.q_stride, a.kv_stride, k_new, a.evict};
   const dim3 grid(a.B * a.S);
   if ((a.D / 2) % 8 == 0)
     rope_append_kernel<T, 8><<<grid, 128, 0, a.stream>>>(p);
@@ -140,8 +146,8 @@ cudaError_t launch_t(const ForwardArgs& a, void* q_rot) {
 
 }  // namespace
 
-cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot) {
-  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_rot) : launch_t<__half>(a, q_rot);
+cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_rot, k_new) : launch_t<__half>(a, q_rot, k_new);
 }
 
 }  // namespace gqa

@@ -25,21 +25,37 @@ def to_device(inp: dict, device="cuda") -> dict:
     return out
 
 
-def run_cuda(inp: dict, stream=None, total=None, workspace_pad=0):
-    """Returns (status, device_status, out[CPU], k_buf[CPU], v_buf[CPU])."""
+def pack_qkv(inp: dict) -> torch.Tensor:
+    """The packed form of the case's new rows: per token its query heads,
+    then its key heads, then its value heads ([B, S, (H + 2 Hkv) * D])."""
     w = inp["workload"]
+    B, S, D = w.batch, w.seq_len, w.head_size
+    parts = [inp["query"].view(B, S, w.num_heads, D), inp["key"].view(B, S, w.kv_num_heads, D),
+             inp["value"].view(B, S, w.kv_num_heads, D)]
+    return torch.cat(parts, dim=2).reshape(B, S, -1).contiguous()
+
+
+def dims_of(inp: dict):
+    w = inp["workload"]
+    bias = inp["attention_bias"]
+    return gqa.make_dims(w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len, w.dtype,
+                         inp.get("rotary_interleaved", 0), 0 if inp["cos"] is None else inp["cos"].shape[0],
+                         1 if bias is None else bias.shape[0], 1 if bias is None else bias.shape[1],
+                         kv_eviction=inp.get("kv_eviction", 0))
+
+
+def run_cuda(inp: dict, stream=None, total=None, workspace_pad=0, packed=False):
+    """Returns (status, device_status, out[CPU], k_buf[CPU], v_buf[CPU]).
+    packed: the new rows go in as one packed query tensor (key, value NULL)."""
     d = to_device(inp)
     out = torch.full_like(d["query"], float("nan"))
-    dims = gqa.make_dims(w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len, w.dtype,
-                         inp.get("rotary_interleaved", 0),
-                         0 if d["cos"] is None else d["cos"].shape[0],
-                         1 if d["attention_bias"] is None else d["attention_bias"].shape[0],
-                         1 if d["attention_bias"] is None else d["attention_bias"].shape[1])
+    dims = dims_of(inp)
     total = inp["total_sequence_length"] if total is None else total
     nbytes = gqa.gqa_workspace_size(dims, total, inp["local_window_size"])
     ws = torch.empty(max(nbytes + workspace_pad, 256), dtype=torch.uint8, device="cuda")
     ws.fill_(0xFF)  # the contents on entry must not matter
-    st = gqa.gqa_forward(dims, d["query"], d["key"], d["value"], d["k_buf"], d["v_buf"], d["k_buf"], d["v_buf"],
+    q, k, v = (pack_qkv(inp).cuda(), None, None) if packed else (d["query"], d["key"], d["value"])
+    st = gqa.gqa_forward(dims, q, k, v, d["k_buf"], d["v_buf"], d["k_buf"], d["v_buf"],
                          d["seqlens_k"], total, d["cos"], d["sin"], inp["scale"], inp["local_window_size"],
                          d["attention_bias"], out, ws, ws.numel(), stream)
     dst = gqa.gqa_check_device_status(stream)
@@ -47,9 +63,12 @@ def run_cuda(inp: dict, stream=None, total=None, workspace_pad=0):
 
 
 def custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999), seed=7, bias=None,
-           window=0, total=None, rotary=True, interleaved=0, sentinel=True):
+           window=0, total=None, rotary=True, interleaved=0, sentinel=True, evict=False):
     """A seeded case of any shape: per-sequence past lengths `past`, past rows
-    N(0, 1), other slots the NaN sentinel; bias (Bb, Hb) ~ N(0, 0.5)."""
+    N(0, 1), other slots the NaN sentinel; bias (Bb, Hb) ~ N(0, 0.5).  With
+    `evict` the call uses the evicting sliding-window cache: a past length
+    may exceed M, and the buffer holds that sequence's min(past, M) most
+    recent rows."""
     w = W.Workload("custom", dtype, B, S, H, Hkv, D, M, 0, 0, bias_shape=bias, local_window_size=window,
                    total_sequence_length=total, rotary=rotary, seed=seed)
     inp = W.make_inputs(w, sentinel=sentinel, fill_past=False)
@@ -57,6 +76,7 @@ def custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999)
     gen = torch.Generator().manual_seed(seed + 1000)
     for name in ("k_buf", "v_buf"):
         for b, n in enumerate(past):
+            n = min(n, M)
             if n > 0:
                 inp[name][b, :, :n] = torch.randn(Hkv, n, D, generator=gen).to(W.DTYPES[dtype])
     t = total if total is not None else max(past) + S
@@ -66,6 +86,7 @@ def custom(dtype="bf16", B=3, S=1, H=8, Hkv=2, D=128, M=1000, past=(0, 517, 999)
     if bias is not None:
         inp["attention_bias"] = (torch.randn(bias[0], bias[1], S, t, generator=gen) * 0.5).to(W.DTYPES[dtype])
     inp["rotary_interleaved"] = interleaved
+    inp["kv_eviction"] = 1 if evict else 0
     return inp
 
 
@@ -82,6 +103,8 @@ def run_oracle(inp: dict, batches=None, heads=None, **kw):
              dtype=w.dtype, batches=batches, heads=heads)
     if inp.get("rotary_interleaved", 0):
         a["interleaved"] = True
+    if inp.get("kv_eviction", 0):
+        a["evict"] = True
     a.update(kw)
     return oracle.gqa_forward(**a)
 

@@ -68,7 +68,7 @@ def dims(**over):
 @pytest.mark.parametrize("bad", [
     dict(batch=0), dict(seq_len=0), dict(num_heads=6, kv_num_heads=4), dict(head_size=12),
     dict(head_size=264), dict(head_size=0), dict(max_seq_len=0), dict(dtype=7), dict(rotary_interleaved=2),
-    dict(kv_num_heads=0),
+    dict(kv_num_heads=0), dict(kv_eviction=2),
 ])
 def test_bad_dims_rejected(lib, bad):
     assert call(dims(**bad)) == gqa.GQA_ERR_INVALID_ARGUMENT
@@ -101,8 +101,12 @@ def test_binding_checks(lib):
 
 
 def test_pointer_checks(lib):
-    assert call(dims(), key=None, value=None) == gqa.GQA_ERR_UNSUPPORTED          # packed QKV
+    # packed QKV (key and value both NULL) passes the pointer checks: the
+    # call fails only at the later scale check
+    assert call(dims(), key=None, value=None, scale=float("nan")) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), key=None, value=None, query=P["q"] + 2) == gqa.GQA_ERR_INVALID_ARGUMENT
     assert call(dims(), key=None) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(), value=None) == gqa.GQA_ERR_INVALID_ARGUMENT
     assert call(dims(), query=None) == gqa.GQA_ERR_INVALID_ARGUMENT
     assert call(dims(), output=None) == gqa.GQA_ERR_INVALID_ARGUMENT
     assert call(dims(), seqlens_k=None) == gqa.GQA_ERR_INVALID_ARGUMENT
@@ -162,8 +166,10 @@ def test_host_entry_workspace_and_checks(lib):
     assert gqa.gqa_workspace_size_host(dims(seq_len=8), 7, 0) == 0
     # checks the host can make come first, in gqa_forward's order
     assert call_host(dims(batch=0)) == gqa.GQA_ERR_INVALID_ARGUMENT
-    assert call_host(d, key=None, value=None) == gqa.GQA_ERR_UNSUPPORTED
-    for bad in (dict(query=None), dict(output=None), dict(seqlens_k=None), dict(key=None),
+    # packed QKV is a valid form here too: these fake addresses fail only as
+    # memory that is not page-locked (before any launch)
+    assert call_host(d, key=None, value=None, workspace_bytes=need) == gqa.GQA_ERR_INVALID_ARGUMENT
+    for bad in (dict(query=None), dict(output=None), dict(seqlens_k=None), dict(key=None), dict(value=None),
                 dict(query=P["q"] + 8), dict(seqlens_k=P["seq"] + 2), dict(workspace=None),
                 dict(workspace_bytes=need - 1), dict(workspace=P["ws"] + 8)):
         assert call_host(d, **{"workspace_bytes": need, **bad}) == gqa.GQA_ERR_INVALID_ARGUMENT, bad
@@ -238,3 +244,24 @@ def test_bound_argument_counts_match_header(lib):
         proto = re.search(r"\b" + name + r"\s*\((.*?)\)\s*;", text, flags=re.S).group(1)
         n = 0 if proto.strip() in ("", "void") else proto.count(",") + 1
         assert len(getattr(lib, name).argtypes) == n, name
+
+
+def test_evicting_cache_host_rules(lib):
+    """kv_eviction = 1: total_sequence_length beyond the buffer is no longer
+    an overflow (the call goes on to the workspace check), the non-shared
+    binding is not taken, and a call that may evict needs the evicting
+    path's scratch (rotated queries and new key rows)."""
+    d = dims(kv_eviction=1, cos_cache_rows=300)
+    need = gqa.gqa_workspace_size(d, 300, 0)
+    assert need >= (2 * 4 * 8 * 64 + 2 * 4 * 2 * 64) * 2
+    assert need > gqa.gqa_workspace_size(d, 128, 0)     # a call that cannot evict takes the plain path
+    assert call(d, total=300, workspace_bytes=need - 1) == gqa.GQA_ERR_INVALID_ARGUMENT
+    assert call(dims(kv_eviction=1), total=300) == gqa.GQA_ERR_INVALID_ARGUMENT   # cos rows < total
+    assert call(dims(cos_cache_rows=300), total=300) == gqa.GQA_ERR_KV_OVERFLOW
+    ns = dict(present_key=0x200000, present_value=0x300000)
+    assert call(dims(kv_eviction=1, past_seq_len=64), **ns) == gqa.GQA_ERR_UNSUPPORTED
+    # the no-alloc entry does not take the evicting cache
+    d1 = dims(kv_eviction=1, seq_len=1, head_size=128)
+    st = gqa.gqa_decode_noalloc(d1, P["q"], P["k"], P["v"], P["kb"], P["vb"], P["kb"], P["vb"], P["seq"], 64,
+                                P["cos"], P["sin"], 0.0, 0, None, P["out"], None)
+    assert st == gqa.GQA_ERR_UNSUPPORTED
