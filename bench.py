@@ -193,7 +193,14 @@ class Problem:
         w = self.w
         self.dims = gqa.make_dims(w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len,
                                   w.dtype, 0, inp["cos"].shape[0] if inp["cos"] is not None else 0,
-                                  *(inp["attention_bias"].shape[:2] if inp["attention_bias"] is not None else (1, 1)))
+                                  *(inp["attention_bias"].shape[:2] if inp["attention_bias"] is not None else (1, 1)),
+                                  kv_eviction=1 if w.kv_eviction else 0)
+        # packed QKV: one query tensor with each token's query, key and value heads
+        self.qkv = None
+        if w.packed:
+            B, S, D = w.batch, w.seq_len, w.head_size
+            self.qkv = torch.cat([inp["query"].view(B, S, w.num_heads, D), inp["key"].view(B, S, w.kv_num_heads, D),
+                                  inp["value"].view(B, S, w.kv_num_heads, D)], dim=2).reshape(B, S, -1).contiguous()
         self.total = inp["total_sequence_length"]
         self.ws_bytes = gqa.gqa_workspace_size(self.dims, self.total, w.local_window_size)
         self.ws = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=device)
@@ -208,7 +215,8 @@ class Problem:
     def step(self, i, stream):
         d = self.inp
         r = i % len(self.kbufs)
-        st = self.gqa.gqa_forward(self.dims, d["query"], d["key"], d["value"], self.kbufs[r], self.vbufs[r],
+        q, k, v = (self.qkv, None, None) if self.qkv is not None else (d["query"], d["key"], d["value"])
+        st = self.gqa.gqa_forward(self.dims, q, k, v, self.kbufs[r], self.vbufs[r],
                                   self.kbufs[r], self.vbufs[r], d["seqlens_k"], self.total, d["cos"], d["sin"],
                                   d["scale"], d["local_window_size"], d["attention_bias"], self.out, self.ws,
                                   self.ws.numel(), stream)
@@ -216,9 +224,12 @@ class Problem:
             raise RuntimeError(self.gqa.gqa_status_string(st))
 
     def launches_per_step(self):
-        # decode: one kernel (append, split-KV attention and the split combine);
-        # prefill: the rotary/append kernel plus the attention kernel
-        return 1 if self.decode else 2
+        # decode: one kernel (append, split-KV attention and the split combine),
+        # plus the eviction kernel on an evicting cache; prefill: the
+        # rotary/append kernel plus the attention kernel
+        if self.decode:
+            return 2 if self.w.kv_eviction else 1
+        return 2
 
 
 def time_steps(prob, steps, warmup, stream, ws_count=1, device=None):
@@ -276,7 +287,7 @@ def e2e_decode(prob, steps, warmup, stream):
         r = i % len(prob.kbufs)
         gqa.forward_host(hq, hk, hv, prob.kbufs[r], prob.vbufs[r], hs, prob.total, w.num_heads, w.kv_num_heads,
                          d["cos"], d["sin"], d["scale"], d["local_window_size"], d["attention_bias"],
-                         output=hout, workspace=wsp, stream=stream)
+                         output=hout, workspace=wsp, stream=stream, kv_eviction=int(w.kv_eviction))
 
     def copy_engine_step(i):
         dq, dk, dv, ds = dviews
@@ -284,7 +295,7 @@ def e2e_decode(prob, steps, warmup, stream):
         dev.copy_(host, non_blocking=True)
         out = gqa.forward(dq, dk, dv, prob.kbufs[r], prob.vbufs[r], ds, prob.total, w.num_heads, w.kv_num_heads,
                           d["cos"], d["sin"], d["scale"], d["local_window_size"], d["attention_bias"],
-                          output=prob.out, workspace=wsp, stream=stream)
+                          output=prob.out, workspace=wsp, stream=stream, kv_eviction=int(w.kv_eviction))
         hout.copy_(out, non_blocking=True)
 
     def timed(step_fn):
@@ -468,7 +479,8 @@ def run_ours(args):
 
     also = []
     if not args.no_also and not args.quick:
-        for other in ("decode_b16", "long_decode", "long_decode_w4096", "prefill_2k", "chunked_prefill"):
+        for other in ("decode_b16", "long_decode", "long_decode_w4096", "prefill_2k", "chunked_prefill",
+                      "decode_b16_packed", "swa_decode_b16"):
             if other == name:
                 continue
             wo = W.CONFIGS[other]

@@ -23,13 +23,18 @@
 //               other tile's work while one tile's softmax runs (ping-pong);
 //   warps 4..7  softmax of tile A, warps 8..11 softmax of tile B (warps 2, 3
 //               idle; the register split favours the softmax warpgroups): thread r owns
-//               query row r (TMEM lane r).  Pass 1 reads the 128 scores of the
-//               row, applies scale, bias and mask (writing adjusted scores back
-//               when there are any) and takes the row max; pass 2 re-reads
-//               them, exponentiates, sums, and writes P (16-bit) over S.  O is
-//               rescaled in TMEM only when the row max grew by more than 2^8
-//               (the un-rescaled terms stay bounded by 2^8 and the final
-//               division uses the same reference max).
+//               query row r (TMEM lane r).  It reads the 128 scores of the row
+//               into registers once, adds the bias and applies the mask there,
+//               takes the row max, exponentiates, sums, and writes P (16-bit)
+//               over S.  O is rescaled in TMEM only when the row max grew by
+//               more than 2^8 (the un-rescaled terms stay bounded by 2^8 and
+//               the final division uses the same reference max).
+// attention_bias shared by the two heads of a CTA (one bias head) with rows
+// of 16-byte multiples: the producer also streams each key tile's bias block
+// [128 query rows x 128 keys] by TMA, as two 64-key halves through a 2-stage
+// ring that both softmax warpgroups read.  Otherwise (a bias per head, or
+// unaligned rows) the bias is added by a separate TMEM pass from global
+// loads.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // With an odd group size the last head of each KV head runs alone (B idle).
 #include <type_traits>
@@ -58,12 +63,19 @@ constexpr int kQBytes = kBM * kD * 2;
 constexpr int kQOff = 0;                   // Q_A, then Q_B
 constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKSt * kTileBytes;
-constexpr int kBarOff = kVOff + kVSt * kTileBytes;
+constexpr int kBiasHalfBytes = kBM * 64 * 2;  // bias block half: [128 query rows x 64 keys]
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain,
-// q_ready
-constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1;
-constexpr int kSlotOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kSlotOff + 16 + 1024;
+// q_ready, bias_full[2], bias_empty[2]
+constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1 + 4;
+// the kernels with a bias also hold the 2-stage bias ring (32 KB) after V
+template <bool kBias>
+struct SmemLayout {
+  static constexpr int kBiasOff = kVOff + kVSt * kTileBytes;
+  static constexpr int kBarOff = kBiasOff + (kBias ? 2 * kBiasHalfBytes : 0);
+  static constexpr int kSlotOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kSlotOff + 16 + 1024;
+};
+static_assert(SmemLayout<true>::kBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThresh = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
 
@@ -80,7 +92,15 @@ struct PrefillParams {
   int n_split;     // key-range splits per work item (1: none)
   float scale_log2;
   int evict;       // sliding-window cache: a full buffer is not an error (no call here evicts)
+  int bias_tma;    // the bias blocks come through the shared-memory ring (bmap)
 };
+
+// First key of a query tile's scan: the window start, rounded down to a
+// multiple of 8 so that every key tile starts on a 16-byte boundary of a bias
+// row (the keys before the window start are masked like any other).
+__host__ __device__ __forceinline__ int scan_start(int past, int i0, int window) {
+  return window > 0 ? (max(0, past + i0 - window + 1) & ~7) : 0;
+}
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
                                             uint32_t bar) {
@@ -96,13 +116,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 template <typename T, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                   const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap bmap,
+                   const PrefillParams p) {
   using E = Elem<T>;
+  using Lay = SmemLayout<kBias>;
   constexpr bool kBF16 = E::is_bf16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t bar0 = sb + kBarOff;
+  const uint32_t bar0 = sb + Lay::kBarOff;
   const uint32_t q_full = bar0;
   const uint32_t k_full = bar0 + 8, k_empty = k_full + 8 * kKSt;
   const uint32_t v_full = k_empty + 8 * kKSt, v_empty = v_full + 8 * kVSt;
@@ -111,8 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t o_done = p_full + 16;         // [A, B]
   const uint32_t drain = o_done + 16;
   const uint32_t q_ready = drain + 8;  // query tiles rotated in shared memory
+  const uint32_t bias_full = q_ready + 8;      // [half 0, half 1]
+  const uint32_t bias_empty = bias_full + 16;  // [half 0, half 1]
   const bool rot = p.cos != nullptr;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
+  const bool bias_tma = kBias && p.bias_tma;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Lay::kSlotOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -135,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i0 = qt * kBM;
   const int i1 = min(i0 + kBM, p.S);
   const int L = past + p.S;
-  const int kstart = p.window > 0 ? max(0, past + i0 - p.window + 1) : 0;
+  const int kstart = scan_start(past, i0, p.window);
   const int kend = past + i1;  // one past the last key any row of the tile sees
   // this CTA's share of the tile's keys: tiles [t_lo, t_lo + n_kv) of n_all
   const int n_all = (kend - kstart + kBN - 1) / kBN;
@@ -168,6 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(q_ready, 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bias_full + 8 * s, 1);
+      mbar_init(bias_empty + 8 * s, 4 * (has_b ? 2 : 1));  // one arrival per softmax warp
+    }
     fence_mbar_init();
   }
   if (warp == 1) tc::alloc(smem_u32(tslot), kTmemCols);
@@ -184,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
+      if (bias_tma) prefetch_tensormap(&bmap);
       mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * kQBytes);
       tma_load_4d(sb + kQOff, &qmap, 0, hA, i0, b, q_full);
       tma_load_4d(sb + kQOff + kBoxBytes, &qmap, 64, hA, i0, b, q_full);
@@ -192,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(sb + kQOff + kQBytes + kBoxBytes, &qmap, 64, hA + 1, i0, b, q_full);
       }
       const int zkv = b * p.Hkv + kh;
-      int issued_k = 0, issued_v = 0;
+      const int zb = p.bias_h > 1 ? hA : 0, wb = p.bias_b > 1 ? b : 0;  // (one bias head when bias_tma)
+      int issued_k = 0, issued_v = 0, issued_b = 0;
       for (int j = 0; j < n_kv; ++j) {
         const int y = kbase + j * kBN;
         const int ks = j % kKSt, vs = j % kVSt;
@@ -201,6 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sb + kKOff + ks * kTileBytes, &kmap, 0, y, zkv, k_full + 8 * ks);
         tma_load_3d(sb + kKOff + ks * kTileBytes + kBoxBytes, &kmap, 64, y, zkv, k_full + 8 * ks);
         issued_k = j + 1;
+        if (bias_tma) {
+          // the tile's bias block (query rows i0.., keys y..), half h into stage h;
+          // y is a multiple of 8 (scan_start), the TMA's 16-byte rule
+          bool stop = false;
+          for (int h = 0; h < 2 && !stop; ++h) {
+            if (j >= 1 && !mbar_wait(bias_empty + 8 * h, (j - 1) & 1, p.err)) stop = true;
+            if (stop) break;
+            mbar_arrive_expect_tx(bias_full + 8 * h, kBiasHalfBytes);
+            tma_load_4d(sb + Lay::kBiasOff + h * kBiasHalfBytes, &bmap, y + 64 * h, i0, zb, wb, bias_full + 8 * h);
+            issued_b = 2 * j + h + 1;
+          }
+          if (stop) break;
+        }
         if (j >= kVSt && !mbar_wait(v_empty + 8 * vs, ((j / kVSt) - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(v_full + 8 * vs, kTileBytes);
         tma_load_3d(sb + kVOff + vs * kTileBytes, &vmap, 0, y, zkv, v_full + 8 * vs);
@@ -213,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(k_full + 8 * (j % kKSt), (j / kKSt) & 1, p.err);
       for (int j = max(0, issued_v - kVSt); j < issued_v; ++j)
         mbar_wait(v_full + 8 * (j % kVSt), (j / kVSt) & 1, p.err);
+      for (int u = max(0, issued_b - 2); u < issued_b; ++u) mbar_wait(bias_full + 8 * (u & 1), (u >> 1) & 1, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -299,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int bb = p.bias_b > 1 ? b : 0, hb = p.bias_h > 1 ? h : 0;
       brow = static_cast<const T*>(p.bias) + (((size_t)bb * p.bias_h + hb) * p.S + i) * p.total;
     }
-    const bool bias_vec = kBias && brow && (p.total % 8 == 0) && (kstart % 8 == 0) &&
+    const bool bias_vec = kBias && !bias_tma && brow && (p.total % 8 == 0) && (kstart % 8 == 0) &&
                           (reinterpret_cast<uintptr_t>(p.bias) & 15) == 0;
     float m_ref = -INFINITY, l_run = 0.f;
     const bool active = t == 0 || has_b;
@@ -380,85 +425,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * t, j & 1, p.err))) { ok = false; break; }
       tc::fence_after();
       const bool edge = (k0 + kBN - 1 > past + i0) || (p.window > 0 && k0 < past + i1 - p.window);
-      const bool adjust = edge || kBias;  // bias and mask applied per score
-      if (adjust) {
-        // Tiles with a mask edge or a bias: rewrite the scores in TMEM, still
-        // in raw units (s + b log2(e) / scale, or -inf where masked), 32
-        // columns at a time; a separate pass keeps this code out of the
-        // common path below.  Column e of the tile is visible when
-        // e <= vis_hi and e > vis_lo.  Without a bias, a chunk that the whole
-        // warp sees is left as it is and one that it cannot see is only
-        // overwritten.
-        const int vis_hi = pos - k0;
-        const int vis_lo = p.window > 0 ? pos - p.window - k0 : -1;
-        constexpr bool has_bias = kBias;
-        // 32 bias values per chunk (16-byte loads), the next chunk's
-        // requested before this chunk is processed
-        auto load_bias = [&](int c, uint4 (&d)[4]) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int key = k0 + c * 32 + q * 8;
-            d[q] = key < kend ? *reinterpret_cast<const uint4*>(brow + key) : make_uint4(0, 0, 0, 0);
-          }
-        };
-        uint4 bcur[4], bnext[4];
-        if (bias_vec) load_bias(0, bcur);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (bias_vec && c < 3) load_bias(c + 1, bnext);
-          const bool all_vis = __all_sync(0xffffffffu, c * 32 + 31 <= vis_hi && c * 32 > vis_lo);
-          const bool none_vis = __all_sync(0xffffffffu, c * 32 > vis_hi || c * 32 + 31 <= vis_lo);
-          if (!has_bias && all_vis) continue;
-          uint32_t r[32];
-          if (none_vis) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(-INFINITY);
-          } else {
-            tc::ld32(tS + c * 32, r);
-            uint32_t bw[16];
-            if (bias_vec) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                bw[4 * q] = bcur[q].x;
-                bw[4 * q + 1] = bcur[q].y;
-                bw[4 * q + 2] = bcur[q].z;
-                bw[4 * q + 3] = bcur[q].w;
-              }
-            } else if (kBias) {
-              // rows past S (no bias row: they add zero), or a bias whose
-              // rows are not 16-byte aligned
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int key = k0 + c * 32 + 2 * e;
-                const float b0 = (brow && key < kend) ? E::to_f(brow[key]) : 0.f;
-                const float b1 = (brow && key + 1 < kend) ? E::to_f(brow[key + 1]) : 0.f;
-                bw[e] = E::pack2(b0, b1);
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) bw[e] = 0u;
-            }
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float2 b2 = E::unpack2(bw[e >> 1]);
-              const float bval = (e & 1) ? b2.y : b2.x;
-              const float v = fmaf(bval, bias_unit, __uint_as_float(r[e]));
-              const bool vis = c * 32 + e <= vis_hi && c * 32 + e > vis_lo;
-              r[e] = __float_as_uint(vis ? v : -INFINITY);
-            }
-          }
-          tc::st32(tS + c * 32, r);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) bcur[q] = bnext[q];
-        }
-        tc::wait_st();
-      }
+      // column e of the tile is visible to this row when vis_lo < e <= vis_hi
+      const int vis_hi = pos - k0;
+      const int vis_lo = p.window > 0 ? pos - p.window - k0 : -1;
       // the row's 128 scores, all in registers (one wait for four loads)
       uint32_t sv[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc::ld32(tS + c * 32, sv[c]);
       tc::wait_ld();
+      if (bias_tma) {
+        // the bias row of this tile from the shared-memory ring (128-byte
+        // swizzled: 16-byte chunk q of row r at chunk q ^ (r & 7)), added in
+        // raw score units: s + b log2(e) / scale
+        bool got = true;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) got = got && mbar_wait(bias_full + 8 * h, j & 1, p.err);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const uint8_t* brow_s = smem + Lay::kBiasOff + row * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = (c & 1) * 4 + q;  // 16-byte chunk of the 64-key half c / 2
+            const uint4 u = *reinterpret_cast<const uint4*>(brow_s + (c >> 1) * kBiasHalfBytes +
+                                                            ((chunk ^ (row & 7)) << 4));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 bv = E::unpack2(w[e]);
+              const int k = q * 8 + 2 * e;
+              sv[c][k] = __float_as_uint(fmaf(bv.x, bias_unit, __uint_as_float(sv[c][k])));
+              sv[c][k + 1] = __float_as_uint(fmaf(bv.y, bias_unit, __uint_as_float(sv[c][k + 1])));
+            }
+          }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bias_empty);
+          mbar_arrive(bias_empty + 8);
+        }
+      } else if (kBias) {
+        // a bias per head, or rows that are not 16-byte multiples: the bias
+        // row of this tile from global memory, 32 keys at a time (0 beyond
+        // the last key any row sees, and on rows past S, which have no bias
+        // row)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t bw[16];
+          if (bias_vec) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int key = k0 + c * 32 + q * 8;  // a multiple of 8, like kend and total
+              const uint4 u = key < kend ? *reinterpret_cast<const uint4*>(brow + key) : make_uint4(0, 0, 0, 0);
+              bw[4 * q] = u.x;
+              bw[4 * q + 1] = u.y;
+              bw[4 * q + 2] = u.z;
+              bw[4 * q + 3] = u.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int key = k0 + c * 32 + 2 * e;
+              const float b0 = (brow && key < kend) ? E::to_f(brow[key]) : 0.f;
+              const float b1 = (brow && key + 1 < kend) ? E::to_f(brow[key + 1]) : 0.f;
+              bw[e] = E::pack2(b0, b1);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 bv = E::unpack2(bw[e]);
+            sv[c][2 * e] = __float_as_uint(fmaf(bv.x, bias_unit, __uint_as_float(sv[c][2 * e])));
+            sv[c][2 * e + 1] = __float_as_uint(fmaf(bv.y, bias_unit, __uint_as_float(sv[c][2 * e + 1])));
+          }
+        }
+      }
+      if (edge) {
+        // the causal (and window) mask, in registers
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int col = c * 32 + e;
+            if (col > vis_hi || col <= vis_lo) sv[c][e] = __float_as_uint(-INFINITY);
+          }
+      }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -619,7 +668,7 @@ __global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParam
   pdl_wait_primary();
   if (!valid || sequence_error(past, p.S, p.M, p.total, p.evict)) return;
   const int qt = i / kBM, i0 = qt * kBM, i1 = min(i0 + kBM, p.S);
-  const int kstart = p.window > 0 ? max(0, past + i0 - p.window + 1) : 0;
+  const int kstart = scan_start(past, i0, p.window);
   const int n_all = (past + i1 - kstart + kBN - 1) / kBN;
   const int ts = (n_all + p.n_split - 1) / p.n_split;
   if (ts >= n_all) return;  // one key range: written directly
@@ -672,6 +721,19 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
         !encode_tensor_map(&vmap, dt, 3, a.vbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  // the bias ring: one bias head for both heads of a CTA, rows of 16-byte
+  // multiples at a 16-byte aligned base (the TMA's rules)
+  CUtensorMap bmap{};
+  const bool bias_tma = a.bias && a.bias_h == 1 && a.total % 8 == 0 &&
+                        (reinterpret_cast<uintptr_t>(a.bias) & 15) == 0;
+  if (bias_tma) {
+    const cuuint64_t dims[4] = {(cuuint64_t)a.total, (cuuint64_t)a.S, 1, (cuuint64_t)a.bias_b};
+    const cuuint64_t strides[3] = {(cuuint64_t)a.total * 2, (cuuint64_t)a.S * a.total * 2,
+                                   (cuuint64_t)a.S * a.total * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kBM, 1, 1};
+    if (!encode_tensor_map(&bmap, dt, 4, const_cast<void*>(a.bias), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   const int n_qt = (a.S + kBM - 1) / kBM;
   const int G = a.H / a.Hkv;
   const int n_pairs = (G + 1) / 2;
@@ -700,15 +762,16 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   p.n_split = n_split;
   p.scale_log2 = a.scale * kLog2e;
   p.evict = a.evict;
+  p.bias_tma = bias_tma ? 1 : 0;
   auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
+  const int smem = a.bias ? SmemLayout<true>::kBytes : SmemLayout<false>::kBytes;
   static std::atomic<int> smem_set[2][kMaxDevices];  // limit set so far, per instantiation and device
   {
-    const cudaError_t e =
-        set_smem_limit(reinterpret_cast<const void*>(kern), kSmemBytes, smem_set[a.bias ? 1 : 0]);
+    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem, smem_set[a.bias ? 1 : 0]);
     if (e != cudaSuccess) return e;
   }
   const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
-  kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, p);
+  kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
   // the split combine, overlapping the attention kernel's tail

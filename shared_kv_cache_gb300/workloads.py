@@ -51,6 +51,8 @@ class Workload:
     total_sequence_length: Optional[int] = None   # None: max_b(past_b) + S
     rotary: bool = True
     seed: int = 0
+    kv_eviction: bool = False       # sliding-window cache: keep the max_seq_len most recent tokens
+    packed: bool = False            # new rows as one packed query tensor [B, S, (H + 2 Hkv) * D]
 
     @property
     def group(self) -> int:
@@ -74,6 +76,13 @@ CONFIGS = {
     "long_decode": Workload("long_decode", "bf16", 8, 1, 64, 8, 128, 32768, 16384, 32767, seed=4),
     "long_decode_w4096": Workload("long_decode_w4096", "bf16", 8, 1, 64, 8, 128, 32768, 16384, 32767,
                                   local_window_size=4096, seed=4),
+    # the batched decode with its new rows in the packed QKV form
+    "decode_b16_packed": Workload("decode_b16_packed", "bf16", 16, 1, 32, 8, 128, 4096, 1, 4095, seed=1,
+                                  packed=True),
+    # the batched decode on a full sliding-window cache (window = capacity =
+    # 4096 slots): every step evicts the oldest token of every sequence
+    "swa_decode_b16": Workload("swa_decode_b16", "bf16", 16, 1, 32, 8, 128, 4096, 4096, 8191,
+                               local_window_size=4096, seed=5, kv_eviction=True),
 }
 
 
@@ -127,7 +136,7 @@ def make_inputs(w: Workload, seed: Optional[int] = None, sentinel: bool = True,
             buf = torch.zeros(B, Hkv, M, D, dtype=t, device=device)
         if fill_past:
             for b in range(B):
-                n = int(past[b])
+                n = min(int(past[b]), M)    # an evicting cache holds at most M rows
                 if n > 0:
                     buf[b, :, :n, :] = randn(Hkv, n, D).to(t)
         bufs.append(buf)
@@ -158,7 +167,10 @@ def bits(t: torch.Tensor):
 
 def decode_bytes(w: Workload, past: torch.Tensor) -> int:
     """Algorithmic bytes of one decode call: the visible K and V rows of every
-    (sequence, KV head), the query and the output, and the appended K/V row."""
+    (sequence, KV head), the query and the output, and the appended K/V row.
+    On an evicting cache see evict_decode_bytes."""
+    if w.kv_eviction:
+        return evict_decode_bytes(w, past)
     e = 2
     L = past.to(torch.int64) + w.seq_len
     if w.local_window_size > 0:
@@ -167,6 +179,26 @@ def decode_bytes(w: Workload, past: torch.Tensor) -> int:
     qo = 2 * w.batch * w.seq_len * w.num_heads * w.head_size * e
     app = 2 * w.batch * w.seq_len * w.kv_num_heads * w.head_size * e
     return kv + qo + app
+
+
+def evict_decode_bytes(w: Workload, past: torch.Tensor) -> int:
+    """Algorithmic bytes of one decode call on the evicting cache: per
+    (sequence, KV head), every cached K and V row that the step must read at
+    least once -- those its token sees and those that move down -- read once,
+    the moved rows written once, plus the query and output and the new row
+    (read from the input, written to its slot)."""
+    e, D, M, W = 2, w.head_size, w.max_seq_len, w.local_window_size
+    row = D * e * 2                                 # one K row and one V row
+    total = 0
+    for pb in past.tolist():
+        n_old = min(pb, M)
+        n_keep = min(pb + 1, M)
+        moved = n_keep - 1 if n_old + 1 > n_keep else 0
+        seen = n_old if W <= 0 else min(n_old, W - 1)   # cached rows inside the window
+        total += w.kv_num_heads * (max(moved, seen) * row + moved * row)
+    total += 2 * w.batch * w.num_heads * D * e      # query in, output out
+    total += 2 * w.batch * w.kv_num_heads * D * e   # new K and V rows written
+    return total
 
 
 def prefill_flops(w: Workload, past: torch.Tensor) -> int:

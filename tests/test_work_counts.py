@@ -54,3 +54,32 @@ def test_prefill_flops_closed_form_for_an_empty_past():
     want = 4 * w.head_size * w.num_heads * w.batch * S * (S + 1) // 2
     assert W.prefill_flops(w, torch.zeros(w.batch, dtype=torch.int32)) == want
     assert abs(want - 1.375e11) / 1.375e11 < 1e-3
+
+
+def test_evicting_decode_bytes_from_the_oracle():
+    """On the evicting cache a step reads every cached row that its token
+    sees or that moves (the union, once), writes the moved rows, and writes
+    the new row.  The moved rows are counted from the oracle's eviction with
+    position-coded rows, the seen ones from the window on absolute positions."""
+    w = W.CONFIGS["swa_decode_b16"].with_(batch=4, max_seq_len=16, local_window_size=6, head_size=8,
+                                          num_heads=4, kv_num_heads=2)
+    past = [3, 15, 16, 40]
+    M, D, e = w.max_seq_len, w.head_size, 2
+    rows_read = rows_moved = 0
+    for pb in past:
+        n_old = oracle.cached_count(pb, M)
+        first = pb - n_old
+        buf = np.zeros((1, 1, M, 1), dtype=np.uint16)
+        buf[0, 0, :n_old, 0] = np.arange(first, pb) + 1         # row = its position + 1
+        new = np.full((1, 1, 1, 1), pb + 1, dtype=np.uint16)
+        out = oracle.evict_keep_recent(buf, new, np.array([pb]))
+        n_keep = min(pb + 1, M)
+        kept_old = set(int(x) - 1 for x in out[0, 0, :n_keep, 0]) - {pb}
+        # a row moves when it stays but changes slot
+        moved = {p for p in kept_old if (p - first) != (p - (pb + 1 - n_keep))}
+        seen = {p for p in range(first, pb) if p > pb - w.local_window_size}
+        rows_read += len(moved | seen)
+        rows_moved += len(moved)
+    want = (w.kv_num_heads * (rows_read + rows_moved) * D * e * 2
+            + 2 * w.batch * w.num_heads * D * e + 2 * w.batch * w.kv_num_heads * D * e)
+    assert W.decode_bytes(w, torch.tensor(past)) == want
