@@ -66,6 +66,8 @@ constexpr int kMail = 4;                     // consumer -> merger mailbox entri
 constexpr size_t kSmPerSM = 233472;          // shared memory per SM (bytes)
 constexpr size_t kSmReservedPerCta = 1024;
 constexpr int kSeqCache = 128;               // seqlens_k entries cached in shared memory
+constexpr int kPrefetchTiles = 4;            // K/V tiles per CTA asked of L2 before the lengths are known
+constexpr int kMergeBatch = 4;               // partials loaded per round of a merge (registers)
 
 // Descriptor of one chunk, written by the producer into a staging slot.
 struct ChunkDesc {
@@ -195,6 +197,9 @@ __device__ __forceinline__ uint32_t epoch_take(unsigned long long* c, uint32_t e
   return (uint32_t)old;
 }
 
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
@@ -341,6 +346,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   pdl_launch_dependents();
+  // While the previous kernel in the stream may still run: warm L2 with the
+  // lengths and with K/V tiles this call will read.  An L2 prefetch only
+  // moves lines into L2, which the previous kernel's writes update, so it
+  // reads nothing before the dependency wait below.  Without a window every
+  // item's keys start at 0: CTA c asks for item c % items, tiles
+  // [kPrefetchTiles * (c / items), ...) (a tile beyond an item's length is
+  // fetched for nothing).
+  if (warp == kProducer && lane == 0) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.seqlens) : "memory");
+    if (p.window == 0 && !p.evicting) {
+      const int items = p.B * p.Hkv;
+      const int item = c % items, t0 = (c / items) * kPrefetchTiles;
+      for (int t = t0; t < t0 + kPrefetchTiles && (t + 1) * kTile <= p.M; ++t) {
+        const size_t off = ((size_t)item * p.M + (size_t)t * kTile) * kD;
+        bulk_prefetch_l2(static_cast<const T*>(p.kbuf) + off, kTile * kD * 2);
+        bulk_prefetch_l2(static_cast<const T*>(p.vbuf) + off, kTile * kD * 2);
+      }
+    }
+  }
   // inputs may be written by the previous kernel in the stream
   pdl_wait_primary();
 
@@ -509,9 +533,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
       const float* ml0 = p.part_ml + (size_t)first * G * 2;
       const float* po0 = p.part_o + (size_t)first * G * kD;
-      // heads four at a time, partials four at a time with a running max: the
-      // loads of a round are independent, so a merge costs about n / 4 round
-      // trips to L2 per head group
+      // heads four at a time, partials kMergeBatch at a time with a running
+      // max: the loads of a round are independent, so a merge costs about
+      // n / kMergeBatch round trips to L2 per head group
       const int d4 = lane * 4;
       for (int g0 = 0; g0 < G; g0 += 4) {
         float mrun[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -519,11 +543,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         float l[4];
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) acc[gi] = make_float4(0.f, 0.f, 0.f, 0.f), l[gi] = 0.f;
-        for (int k0 = 0; k0 < n; k0 += 4) {
-          float4 ov[4][4];
-          float2 mlv[4][4];
+        for (int k0 = 0; k0 < n; k0 += kMergeBatch) {
+          float4 ov[kMergeBatch][4];
+          float2 mlv[kMergeBatch][4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
+          for (int q = 0; q < kMergeBatch; ++q)
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
               const int k = k0 + q, g = g0 + gi;
@@ -537,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int gi = 0; gi < 4; ++gi) {
             float mb = mrun[gi];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) mb = fmaxf(mb, mlv[q][gi].x);
+            for (int q = 0; q < kMergeBatch; ++q) mb = fmaxf(mb, mlv[q][gi].x);
             const float base = mb == -INFINITY ? 0.f : mb;
             const float sc = fast_exp2(mrun[gi] - base);  // 0 while nothing has been added
             mrun[gi] = mb;
@@ -547,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             acc[gi].z *= sc;
             acc[gi].w *= sc;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kMergeBatch; ++q) {
               const float w = fast_exp2(mlv[q][gi].x - base);
               l[gi] += w * mlv[q][gi].y;
               acc[gi].x += w * ov[q][gi].x;
