@@ -5,9 +5,10 @@
 // run from the window start lo_b to the true length L_b = past_b + 1; the scan
 // stops there and never sweeps max_seq_len ("KV Cache", rocMLIR discussion,
 // "Short summary of notes").  Those keys are cut into 64-key tiles, and each
-// item's tiles into chunks of C tiles, C chosen so that there are about
-// chunks_per_cta chunks per CTA of the persistent grid (about two CTAs per
-// SM).  CTA c starts on chunk c; every further chunk is handed out by an
+// item's tiles into chunks of C tiles, C chosen so that there are about one
+// (short calls) or chunks_per_cta (long calls) chunks per CTA of the
+// persistent grid (about two CTAs per SM; see chunk_target).  CTA c starts on
+// chunk c; every further chunk is handed out by an
 // atomic ticket, so CTAs that the memory system serves faster take more
 // chunks and all of them finish together.
 //
@@ -66,7 +67,11 @@ constexpr int kMail = 4;                     // consumer -> merger mailbox entri
 constexpr size_t kSmPerSM = 233472;          // shared memory per SM (bytes)
 constexpr size_t kSmReservedPerCta = 1024;
 constexpr int kSeqCache = 128;               // seqlens_k entries cached in shared memory
-constexpr int kPrefetchTiles = 4;            // K/V tiles per CTA asked of L2 before the lengths are known
+#ifndef GQA_PREFETCH_TILES
+#define GQA_PREFETCH_TILES 4
+#endif
+constexpr int kPrefetchTiles = GQA_PREFETCH_TILES;            // K/V tiles per CTA asked of L2 before the lengths are known
+constexpr int kShortTilesPerCta = 24;        // see chunk_target
 constexpr int kMergeBatch = 4;               // partials loaded per round of a merge (registers)
 
 // Descriptor of one chunk, written by the producer into a staging slot.
@@ -206,6 +211,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+// Chunks the partition aims at for T tiles in all.  A short call (at most
+// kShortTilesPerCta tiles per CTA on average) takes one chunk per CTA: each
+// chunk boundary and each split item's merge costs more than the balance that
+// more chunks buy there.  Longer calls take p.chunks_per_cta chunks per CTA, so
+// that the chunk tickets can even out the CTAs' end times.
+__device__ __forceinline__ int chunk_target(const DynParams& p, int T) {
+  return T <= kShortTilesPerCta * p.P ? p.P : p.chunks_per_cta * p.P;
+}
+
 // The partition, computed identically by every producer warp: per-sequence
 // tile counts, the chunk size C and the chunk count U.
 struct Partition {
@@ -219,7 +233,7 @@ __device__ Partition make_partition(const DynParams& p, const int* sl, int lane)
     T += warp_sum(b < p.B ? seq_tiles(p, sl[b], lo, L) : 0);
   }
   T *= p.Hkv;
-  const int target = p.chunks_per_cta * p.P;
+  const int target = chunk_target(p, T);
   const int C = max(2, (T + target - 1) / target);
   int U = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -264,7 +278,7 @@ __device__ ChunkDesc partition_and_locate_small(const DynParams& p, const int* s
   int lo = 0, L = 0;
   const int tb = lane < p.B ? seq_tiles(p, sl[lane], lo, L) : 0;
   const int T = warp_sum(tb) * p.Hkv;
-  const int target = p.chunks_per_cta * p.P;
+  const int target = chunk_target(p, T);
   pt.C = max(2, (T + target - 1) / target);
   const int nb = (tb + pt.C - 1) / pt.C;
   const int ch = nb * p.Hkv;
