@@ -452,10 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 bv = E::unpack2(w[e]);
               const int k = q * 8 + 2 * e;
-              sv[c][k] = __float_as_uint(fmaf(bv.x, bias_unit, __uint_as_float(sv[c][k])));
-              sv[c][k + 1] = __float_as_uint(fmaf(bv.y, bias_unit, __uint_as_float(sv[c][k + 1])));
+              const float2 r = fma2(E::unpack2(w[e]), make_float2(bias_unit, bias_unit),
+                                    make_float2(__uint_as_float(sv[c][k]), __uint_as_float(sv[c][k + 1])));
+              sv[c][k] = __float_as_uint(r.x);
+              sv[c][k + 1] = __float_as_uint(r.y);
             }
           }
         __syncwarp();
@@ -492,9 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float2 bv = E::unpack2(bw[e]);
-            sv[c][2 * e] = __float_as_uint(fmaf(bv.x, bias_unit, __uint_as_float(sv[c][2 * e])));
-            sv[c][2 * e + 1] = __float_as_uint(fmaf(bv.y, bias_unit, __uint_as_float(sv[c][2 * e + 1])));
+            const float2 r = fma2(E::unpack2(bw[e]), make_float2(bias_unit, bias_unit),
+                                  make_float2(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])));
+            sv[c][2 * e] = __float_as_uint(r.x);
+            sv[c][2 * e + 1] = __float_as_uint(r.y);
           }
         }
       }
@@ -508,11 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col > vis_hi || col <= vis_lo) sv[c][e] = __float_as_uint(-INFINITY);
           }
       }
+      // the row max, two scores per instruction on four independent chains
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sv[c][e]));
+        for (int e = 0; e < 32; e += 2)
+          mx[(e >> 1) & 3] = max3(mx[(e >> 1) & 3], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
       // (scale > 0: the max of the scaled scores)
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
       // running max with lazy rescaling of O (the rescale itself is done
@@ -529,7 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // score is already in registers)
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       const float sc = p.scale_log2;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // exponent arguments, and the row sum, two lanes per instruction
+      const float2 sc2 = make_float2(sc, sc), nmu2 = make_float2(-mu, -mu);
+      float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // (two instantiations, so that the common case carries no residue code)
       auto make_p = [&](auto split_c) {
         constexpr bool kSplit = decltype(split_c)::value;
@@ -538,11 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float x0 = fmaf(__uint_as_float(sv[c][2 * e]), sc, -mu);
-            const float x1 = fmaf(__uint_as_float(sv[c][2 * e + 1]), sc, -mu);
-            const float a = fast_exp2(x0);
-            const float bb = fast_exp2(x1);
-            rs[e & 3] += a + bb;
+            const float2 x = fma2(make_float2(__uint_as_float(sv[c][2 * e]), __uint_as_float(sv[c][2 * e + 1])), sc2,
+                                  nmu2);
+            const float a = fast_exp2(x.x);
+            const float bb = fast_exp2(x.y);
+            rs2[e & 1] = add2(rs2[e & 1], make_float2(a, bb));
             pk[e] = E::pack2(a, bb);
             if (kSplit) {  // keep P in fp32 for its rounding residue below
               sv[c][2 * e] = __float_as_uint(a);
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         make_p(std::true_type{});
       else
         make_p(std::false_type{});
-      l_run += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      l_run += (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
       if (any_need && j > 0) {
         // O_t holds the earlier tiles' sum once P_t(j-1) V_(j-1) has completed
         // (o_done_t is then at phase j - 1 or j: S_t(j) was issued after it)
@@ -652,9 +658,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merges the key-range splits of the work items that were split: per output
 // row (b, i, h), with partials (O_s, m_s, l_s) of the splits s that had keys,
 //   m* = max m_s,  o = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s.
-// One warp per row, four dimensions per lane; rows of unsplit items were
-// written by the attention kernel and are skipped.  The lengths are read
-// before waiting for the attention kernel (they are inputs).
+// One warp per row, four dimensions per lane; the loads of up to kCombineBatch
+// splits are issued together (one round trip to L2 per batch).  Rows of
+// unsplit items were written by the attention kernel and are skipped.  The
+// lengths are read before waiting for the attention kernel (they are inputs).
+constexpr int kCombineBatch = 8;
 template <typename T>
 __global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParams p) {
   using E = Elem<T>;
@@ -677,21 +685,39 @@ __global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParam
   const int item = qt * (p.B * p.Hkv * p.n_pairs) + (b * p.Hkv + kh) * p.n_pairs + pr;
   const int row = i - i0;
   auto prow = [&](int s) { return (((size_t)item * p.n_split + s) * 2 + t) * kBM + row; };
-  float ms = -INFINITY;
-  for (int s = 0; s < n_eff; ++s) ms = fmaxf(ms, p.part_ml[prow(s) * 2]);
-  const float base = ms == -INFINITY ? 0.f : ms;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float l = 0.f;
   const int d4 = lane * 4;
-  for (int s = 0; s < n_eff; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + prow(s) * 2);
-    const float4 o = *reinterpret_cast<const float4*>(p.part_o + prow(s) * kD + d4);
-    const float w = fast_exp2(ml.x - base);
-    l += w * ml.y;
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
+  float m_run = -INFINITY, l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < n_eff; s0 += kCombineBatch) {
+    float2 ml[kCombineBatch];
+    float4 o[kCombineBatch];
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) {
+      const bool v = s0 + k < n_eff;
+      ml[k] = v ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + prow(s0 + k) * 2)) : make_float2(-INFINITY, 0.f);
+      o[k] = v ? __ldcg(reinterpret_cast<const float4*>(p.part_o + prow(s0 + k) * kD + d4))
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mb = m_run;
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) mb = fmaxf(mb, ml[k].x);
+    const float base = mb == -INFINITY ? 0.f : mb;
+    const float sc = fast_exp2(m_run - base);  // 0 while nothing has been added
+    m_run = mb;
+    l *= sc;
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k) {
+      const float w = fast_exp2(ml[k].x - base);
+      l += w * ml[k].y;
+      acc.x += w * o[k].x;
+      acc.y += w * o[k].y;
+      acc.z += w * o[k].z;
+      acc.w += w * o[k].w;
+    }
   }
   const float inv = 1.f / l;
   uint2 packed;
@@ -789,16 +815,21 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
 
 }  // namespace
 
+#ifndef GQA_PREFILL_SPLIT_FACTOR
+#define GQA_PREFILL_SPLIT_FACTOR 3
+#endif
+constexpr int kSplitFactor = GQA_PREFILL_SPLIT_FACTOR;
+
 int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms) {
   // A grid of fewer than two CTAs per SM cuts the key range of each query
-  // tile into up to 3 * SMs / CTAs pieces (no more than it has key tiles),
-  // so that the long key ranges do not set the time.
+  // tile into up to kSplitFactor * SMs / CTAs pieces (no more than it has key
+  // tiles), so that the long key ranges do not set the time.
   const int n_qt = (S + kBM - 1) / kBM;
   const int G = H / Hkv;
   const long long base = (long long)B * Hkv * ((G + 1) / 2) * n_qt;
   if (base >= 2ll * num_sms) return 1;
   const int max_tiles = (total + kBN - 1) / kBN + 1;
-  const int want = (int)((3ll * num_sms + base - 1) / base);
+  const int want = (int)(((long long)kSplitFactor * num_sms + base - 1) / base);
   return want < 1 ? 1 : (want > max_tiles ? max_tiles : want);
 }
 size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split) {
