@@ -242,6 +242,29 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// rotate_pair on two pairs at once: the same four products and two sums in
+// fp32, each rounded to nearest (explicit .rn, never contracted), so the
+// results are bit-identical to rotate_pair's
+__device__ __forceinline__ void rotate_pair2(float2 x1, float2 x2, float2 c, float2 s, float2& y1, float2& y2) {
+  y1 = sub2(mul2(x1, c), mul2(x2, s));
+  y2 = add2(mul2(x2, c), mul2(x1, s));
+}
 // max(a, b, c) in one instruction
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;

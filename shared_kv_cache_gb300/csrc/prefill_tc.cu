@@ -111,6 +111,64 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Rotary embedding of query row `row` of a tile in shared memory: the
+// rotation of the append kernel (two pairs per packed instruction, the same
+// roundings), applied to the 128-byte-swizzled tile (element j of a row sits
+// in box j / 64, 16-byte chunk (j % 64) / 8, chunk slot chunk ^ (row % 8)).
+// cq/sq: the position's cos and sin rows (64 values each).
+template <typename T>
+__device__ __forceinline__ void rotate_query_row(uint8_t* qrow, int row, const uint4 (&cq)[8], const uint4 (&sq)[8],
+                                                 bool interleaved) {
+  using E = Elem<T>;
+  auto w32 = [](const uint4& u, int k) { return k == 0 ? u.x : k == 1 ? u.y : k == 2 ? u.z : u.w; };
+  if (!interleaved) {
+    // pairs (j, j + 64): chunk c of box 0 with chunk c of box 1
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int so = (c ^ (row & 7)) << 4;
+      uint4* p1 = reinterpret_cast<uint4*>(qrow + so);
+      uint4* p2 = reinterpret_cast<uint4*>(qrow + kBoxBytes + so);
+      const uint4 x1 = *p1, x2 = *p2;
+      uint32_t y1[4], y2[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {  // elements 2k, 2k + 1 of the chunk
+        float2 a, b;
+        rotate_pair2(E::unpack2(w32(x1, k)), E::unpack2(w32(x2, k)), E::unpack2(w32(cq[c], k)),
+                     E::unpack2(w32(sq[c], k)), a, b);
+        y1[k] = E::pack2(a.x, a.y);
+        y2[k] = E::pack2(b.x, b.y);
+      }
+      *p1 = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+      *p2 = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+    }
+  } else {
+    // pairs (2j, 2j + 1) inside each chunk: chunk c of box bx holds pairs
+    // j = 32 bx + 4 c .. + 3, whose cos/sin are the words 2 (c & 1), +1 of
+    // chunk 4 bx + c / 2 of the cache row
+#pragma unroll
+    for (int bx = 0; bx < 2; ++bx)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4* pc = reinterpret_cast<uint4*>(qrow + bx * kBoxBytes + ((c ^ (row & 7)) << 4));
+        const uint4 x = *pc;
+        const uint4& cc = cq[4 * bx + (c >> 1)];
+        const uint4& ss = sq[4 * bx + (c >> 1)];
+        uint32_t y[4];
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {  // pairs k, k + 1 of the chunk
+          const float2 xa = E::unpack2(w32(x, k)), xb = E::unpack2(w32(x, k + 1));
+          const float2 cs = E::unpack2(w32(cc, 2 * (c & 1) + (k >> 1)));
+          const float2 sn = E::unpack2(w32(ss, 2 * (c & 1) + (k >> 1)));
+          float2 a, b;
+          rotate_pair2(make_float2(xa.x, xb.x), make_float2(xa.y, xb.y), cs, sn, a, b);
+          y[k] = E::pack2(a.x, b.x);
+          y[k + 1] = E::pack2(a.y, b.y);
+        }
+        *pc = make_uint4(y[0], y[1], y[2], y[3]);
+      }
+  }
+}
+
 // kBias: the call has an attention_bias (a separate instantiation, so that
 // calls without one carry no bias code)
 template <typename T, bool kBias>
@@ -367,54 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (__all_sync(0xffffffffu, mbar_wait(q_full, 0, p.err)) && do_row) {
-        uint8_t* qrow = smem + kQOff + t * kQBytes + row * 128;
-        auto half8 = [](const uint4& u, int k) {  // 16-bit element k (0..7) of a 16-byte chunk
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          const float2 f = E::unpack2(w[k >> 1]);
-          return (k & 1) ? f.y : f.x;
-        };
-        if (!p.interleaved) {
-          // pairs (j, j + 64): chunk c of box 0 with chunk c of box 1
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int so = ((c ^ (row & 7)) << 4);
-            uint4* p1 = reinterpret_cast<uint4*>(qrow + so);
-            uint4* p2 = reinterpret_cast<uint4*>(qrow + kBoxBytes + so);
-            const uint4 x1 = *p1, x2 = *p2;
-            uint32_t y1[4], y2[4];
-#pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-              float a0, b0, a1, b1;
-              rotate_pair(half8(x1, k), half8(x2, k), half8(cq[c], k), half8(sq[c], k), a0, b0);
-              rotate_pair(half8(x1, k + 1), half8(x2, k + 1), half8(cq[c], k + 1), half8(sq[c], k + 1), a1, b1);
-              y1[k >> 1] = E::pack2(a0, a1);
-              y2[k >> 1] = E::pack2(b0, b1);
-            }
-            *p1 = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-            *p2 = make_uint4(y2[0], y2[1], y2[2], y2[3]);
-          }
-        } else {
-          // pairs (2j, 2j + 1) inside each chunk: chunk c of box b holds
-          // pairs j = 32 b + 4 c .. + 3
-#pragma unroll
-          for (int bx = 0; bx < 2; ++bx)
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              uint4* pc = reinterpret_cast<uint4*>(qrow + bx * kBoxBytes + ((c ^ (row & 7)) << 4));
-              const uint4 x = *pc;
-              const int j0 = 32 * bx + 4 * c;
-              uint32_t y[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const int j = j0 + k;
-                float a, bb;
-                rotate_pair(half8(x, 2 * k), half8(x, 2 * k + 1), half8(cq[j >> 3], j & 7), half8(sq[j >> 3], j & 7),
-                            a, bb);
-                y[k] = E::pack2(a, bb);
-              }
-              *pc = make_uint4(y[0], y[1], y[2], y[3]);
-            }
-        }
+        rotate_query_row<T>(smem + kQOff + t * kQBytes + row * 128, row, cq, sq, p.interleaved != 0);
         fence_proxy_async_smem();  // visible to the tensor core's reads
       }
       mbar_arrive(q_ready);
