@@ -46,21 +46,23 @@
 // slots, and the new row is only patched into shared memory: the buffer is
 // rewritten afterwards by the eviction kernel, once every read is done.
 #include "common.cuh"
+#include "decode_tile.cuh"
 #include "internal.h"
 
 namespace gqa {
 namespace {
 
-constexpr int kD = 128;
-constexpr int kTile = kDecodeTile;           // keys per stage
-constexpr int kCW = 4;                       // consumer warps (16 keys each)
+using dtile::kBoxBytes;
+using dtile::kCW;                            // consumer warps (16 keys each)
+using dtile::kD;
+using dtile::kQStride;
+using dtile::kStageBytes;
+using dtile::kTile;                          // keys per stage
+using dtile::kTileBytes;
+using dtile::sw_off;
 constexpr int kStages = 3;
 constexpr int kThreads = (kCW + 2) * 32;  // consumers, producer, merger
 constexpr int kProducer = kCW, kMerger = kCW + 1;  // warp indices
-constexpr int kBoxBytes = kTile * 128;       // one 64-column box of a tile
-constexpr int kTileBytes = 2 * kBoxBytes;    // K (or V) tile, 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;  // K + V
-constexpr int kQStride = kD + 8;             // padded query row (elements)
 constexpr int kRing = kStages * kStageBytes;
 constexpr int kSlots = 2;                    // descriptor / staging slots
 constexpr int kMail = 4;                     // consumer -> merger mailbox entries
@@ -101,7 +103,7 @@ struct Layout {
 };
 __host__ __device__ constexpr Layout layout_for(int G) {
   const int nt = G <= 8 ? 1 : 2;                        // 8-head column tiles
-  const int w = nt * (8 * 4 * 32 * 4 + 4 * 32 * 4);     // O^T fragments + (m, l) pairs, per lane
+  const int w = dtile::hand_off_bytes(nt);              // O^T fragments + (m, l) pairs
   int merge = 2 * w;
   const int qbytes = 16 * kQStride * 2;
   if (merge < qbytes) merge = qbytes;
@@ -145,12 +147,6 @@ struct DynParams {
   uint32_t epoch;
   float scale_log2;
 };
-
-// Byte offset of 16-byte chunk c (0..15) of row r inside a [kTile x 128]
-// tile held as two 128-byte-wide boxes, each with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t sw_off(int r, int c) {
-  return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 // Keys of sequence b: [lo, L); returns its tile count (0 when the sequence
 // fails the length check and is skipped).
@@ -611,7 +607,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   // ---------------- consumers (warps 0..3, 128 threads) ----------------
-  const int gq = lane >> 2, tq = lane & 3;  // fragment row / column group
   const bool rot = p.cos != nullptr;
   const bool inter = p.interleaved != 0;
   int gt = 0;  // tiles consumed by this CTA
@@ -653,118 +648,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     //    zero), from the staging slot
     named_bar_sync(1, kCW * 32);  // the previous chunk's merge reads are done
     {
-      using V8 = VecT<T, 8>;
-      const int g = tid >> 3, j0 = (tid & 7) * 8;
-      auto rotate8 = [&](const T* src, V8& y1, V8& y2) {
-        V8 x1, x2;
-        if (!inter) {
-          x1 = *reinterpret_cast<const V8*>(src + j0);
-          x2 = *reinterpret_cast<const V8*>(src + kD / 2 + j0);
-        } else {
-          const V8 xa = *reinterpret_cast<const V8*>(src + 2 * j0);
-          const V8 xb = *reinterpret_cast<const V8*>(src + 2 * j0 + 8);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            x1.v[e] = xa.v[2 * e];
-            x2.v[e] = xa.v[2 * e + 1];
-            x1.v[e + 4] = xb.v[2 * e];
-            x2.v[e + 4] = xb.v[2 * e + 1];
-          }
-        }
-        if (rot) {
-          const V8 cv = *reinterpret_cast<const V8*>(st_c + j0);
-          const V8 sv = *reinterpret_cast<const V8*>(st_s + j0);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float a, cc;
-            rotate_pair(E::to_f(x1.v[e]), E::to_f(x2.v[e]), E::to_f(cv.v[e]), E::to_f(sv.v[e]), a, cc);
-            y1.v[e] = E::from_f(a);
-            y2.v[e] = E::from_f(cc);
-          }
-        } else {
-          y1 = x1;
-          y2 = x2;
-        }
-      };
-      auto store8 = [&](T* dst, const V8& y1, const V8& y2) {
-        if (!inter) {
-          *reinterpret_cast<V8*>(dst + j0) = y1;
-          *reinterpret_cast<V8*>(dst + kD / 2 + j0) = y2;
-        } else {
-          V8 ya, yb;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            ya.v[2 * e] = y1.v[e];
-            ya.v[2 * e + 1] = y2.v[e];
-            yb.v[2 * e] = y1.v[e + 4];
-            yb.v[2 * e + 1] = y2.v[e + 4];
-          }
-          *reinterpret_cast<V8*>(dst + 2 * j0) = ya;
-          *reinterpret_cast<V8*>(dst + 2 * j0 + 8) = yb;
-        }
-      };
-      for (int gg = g; gg < 8 * NT; gg += 16) {
-        V8 y1, y2;
-        if (gg < G) {
-          rotate8(st_qp + gg * kD, y1, y2);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) y1.v[e] = y2.v[e] = E::from_f(0.f);
-        }
-        store8(qs + gg * kQStride, y1, y2);
-      }
-      if (has_new) {
-        // the append: rotated new key row and raw value row into slot `past`
-        const size_t row = (((size_t)b * p.Hkv + kh) * p.M + past) * kD;
-        if (tid < 8) {
-          V8 k1, k2;
-          rotate8(st_k, k1, k2);
-          store8(news, k1, k2);
-          if (!p.evicting) store8(static_cast<T*>(p.kbuf) + row, k1, k2);
-        } else if (tid < 24) {
-          const int dd = (tid - 8) * 8;
-          const V8 vv = *reinterpret_cast<const V8*>(st_v + dd);
-          *reinterpret_cast<V8*>(news + kD + dd) = vv;
-          if (!p.evicting) *reinterpret_cast<V8*>(static_cast<T*>(p.vbuf) + row + dd) = vv;
-        }
-      }
+      // the append into slot `past` (an evicting call's buffer is rewritten
+      // after the attention instead)
+      const bool append = has_new && !p.evicting;
+      const size_t row = (((size_t)b * p.Hkv + kh) * p.M + past) * kD;
+      dtile::prepare_rows<T, NT>(tid, G, st_qp, rot ? st_c : nullptr, st_s, st_k, st_v, inter, qs, has_new, news,
+                                 append ? static_cast<T*>(p.kbuf) + row : nullptr,
+                                 append ? static_cast<T*>(p.vbuf) + row : nullptr);
     }
     named_bar_sync(1, kCW * 32);  // rotated rows ready; the staging slot is free
     if (lane == 0) mbar_arrive(bar_dempty + 8 * ds);
 
-    // bias rows of this thread's heads (8*nt + 2*tq + e)
-    const T* brow[NT][2];
-    {
-      const int bb = p.bias_b > 1 ? b : 0;
-      const T* bbase = p.bias ? static_cast<const T*>(p.bias) + (size_t)bb * p.bias_h * p.total : nullptr;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int hd = 8 * nt + 2 * tq + e;
-          brow[nt][e] = (bbase && hd < G) ? bbase + (size_t)(p.bias_h > 1 ? kh * G + hd : 0) * p.total : nullptr;
-        }
-    }
-    // query B-fragments (d x heads), kept in registers for the whole chunk
-    uint32_t qb[NT][8][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const uint32_t qrow = smem_u32(qs + (8 * nt + (lane & 7)) * kQStride);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        ldsm_x4(qrow + (4 * j + (lane >> 3)) * 16, qb[nt][2 * j][0], qb[nt][2 * j][1], qb[nt][2 * j + 1][0],
-                qb[nt][2 * j + 1][1]);
-    }
-
-    // O^T accumulators: d-tile md (rows d = 16 md + gq, +8) x heads (2 tq, 2 tq + 1)
-    float o[NT][8][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[nt][i][0] = o[nt][i][1] = o[nt][i][2] = o[nt][i][3] = 0.f;
-    float mh[NT][2], lh[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mh[nt][0] = mh[nt][1] = -INFINITY, lh[nt][0] = lh[nt][1] = 0.f;
+    dtile::ChunkAcc<T, NT> acc;
+    acc.begin(qs, lane, G, b, kh, p.bias, p.bias_b, p.bias_h, p.total);
 
     bool ok = true;
     for (int t = t0; t < t1; ++t, ++gt) {
@@ -776,108 +672,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t kst = sbase + st * kStageBytes;
       const uint32_t vst = kst + kTileBytes;
       const int tk0 = klo + t * kTile;  // first key of the tile
-      const int wr0 = warp * 16;        // first tile row of this warp
-      bool touched = false;
-      if (has_new && t == tb - 1) {
-        const int r = past - tk0;
-        if ((r >> 4) == warp) {
-          const int cch = lane & 15;
-          const uint4 val = *reinterpret_cast<const uint4*>(news + (lane < 16 ? 0 : kD) + cch * 8);
-          *reinterpret_cast<uint4*>(smem + ((lane < 16 ? kst : vst) - sbase + sw_off(r, cch))) = val;
-          touched = true;
-        }
-      }
-      if (tk0 + wr0 + 16 > L) {
-        // value rows beyond the length: zero them, so that P = 0 meets finite V
-        const int rz = max(L - tk0, wr0);
-        const int n = (wr0 + 16 - rz) * 16;
-        for (int idx = lane; idx < n; idx += 32)
-          *reinterpret_cast<uint4*>(smem + (vst - sbase) + sw_off(rz + (idx >> 4), idx & 15)) =
-              make_uint4(0, 0, 0, 0);
-        touched = true;
-      }
-      __syncwarp();
-
-      // S^T = K Q^T: 16 keys (rows) x 8 heads (columns) per n-tile
-      float sc[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-      {
-        const int mi = lane >> 3;
-        const int kr = wr0 + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          uint32_t a[4];
-          ldsm_x4(kst + sw_off(kr, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_16816<kBF16>(sc[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
-        }
-      }
-      // scale, bias, mask; the thread's keys are gq and gq + 8 of the warp's 16
-      const int key0 = tk0 + wr0 + gq;
-      uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = key0 + (e >> 1) * 8;
-          float v = sc[nt][e] * p.scale_log2;
-          const T* br = brow[nt][e & 1];
-          if (br && key < L) v = fmaf(E::to_f(br[key]), kLog2e, v);
-          sc[nt][e] = key < L ? v : -INFINITY;
-        }
-        float mx[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float m = fmaxf(sc[nt][e], sc[nt][e + 2]);
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-          const float mn = fmaxf(mh[nt][e], m);
-          const float mu = mn == -INFINITY ? 0.f : mn;
-          mx[e] = mu;
-          const float corr = fast_exp2(mh[nt][e] - mu);
-          mh[nt][e] = mn;
-          lh[nt][e] *= corr;
-#pragma unroll
-          for (int md = 0; md < 8; ++md) {
-            o[nt][md][e] *= corr;
-            o[nt][md][e + 2] *= corr;
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] = fast_exp2(sc[nt][e] - mx[e & 1]);
-        lh[nt][0] += sc[nt][0] + sc[nt][2];
-        lh[nt][1] += sc[nt][1] + sc[nt][3];
-        // P^T (keys x heads) -> B fragments: transpose the two 8x8 halves.
-        // Short items also carry P's rounding residue (P = hi + lo, both
-        // 16-bit), so that P.V keeps fp32-level accuracy where a few keys
-        // dominate the output.
-        const uint32_t h0 = E::pack2(sc[nt][0], sc[nt][1]);
-        const uint32_t h1 = E::pack2(sc[nt][2], sc[nt][3]);
-        bh[nt][0] = movmatrix_trans(h0);
-        bh[nt][1] = movmatrix_trans(h1);
-        if (splitp) {
-          const float2 f0 = E::unpack2(h0), f1 = E::unpack2(h1);
-          bl[nt][0] = movmatrix_trans(E::pack2(sc[nt][0] - f0.x, sc[nt][1] - f0.y));
-          bl[nt][1] = movmatrix_trans(E::pack2(sc[nt][2] - f1.x, sc[nt][3] - f1.y));
-        }
-      }
-      // O^T += V^T P^T over this warp's 16 keys
-      {
-        const int mi = lane >> 3;
-        const int vr = wr0 + ((mi >> 1) << 3) + (lane & 7);
-#pragma unroll
-        for (int md = 0; md < 8; ++md) {
-          uint32_t a[4];
-          ldsm_x4_t(vst + sw_off(vr, 2 * md + (mi & 1)), a[0], a[1], a[2], a[3]);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_16816<kBF16>(o[nt][md], a, bh[nt][0], bh[nt][1]);
-            if (splitp) mma_16816<kBF16>(o[nt][md], a, bl[nt][0], bl[nt][1]);
-          }
-        }
-      }
+      const bool touched =
+          acc.patch(smem, sbase, kst, vst, warp, lane, tk0, L, has_new && t == tb - 1, past, news);
+      acc.tile(kst, vst, warp, lane, tk0, L, p.scale_log2, splitp);
       __syncwarp();
       if (lane == 0) {
         if (touched) fence_proxy_async_smem();
@@ -886,109 +683,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // -- merge the four warps' (O^T, m, l) in two rounds through shared memory
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float l = lh[nt][e];
-        l += __shfl_xor_sync(0xffffffffu, l, 4);
-        l += __shfl_xor_sync(0xffffffffu, l, 8);
-        l += __shfl_xor_sync(0xffffffffu, l, 16);
-        lh[nt][e] = l;
-      }
+    acc.reduce_sums();
     // every warp is done reading the ring and the query rows; leave together
     // if any wait ran out
     if (!named_bar_and(1, kCW * 32, ok)) break;
     float* mw = reinterpret_cast<float*>(smem + lay.merge_off);
-    const int wfl = lay.merge_warp_bytes / 4;  // floats per hand-off slot
-    auto hand_off = [&](float* dst) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int md = 0; md < 8; ++md)
-          *reinterpret_cast<float4*>(dst + ((nt * 8 + md) * 32 + lane) * 4) =
-              make_float4(o[nt][md][0], o[nt][md][1], o[nt][md][2], o[nt][md][3]);
-        *reinterpret_cast<float4*>(dst + NT * 8 * 128 + (nt * 32 + lane) * 4) =
-            make_float4(mh[nt][0], lh[nt][0], mh[nt][1], lh[nt][1]);
-      }
-    };
-    auto absorb = [&](const float* src) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float4 ml = *reinterpret_cast<const float4*>(src + NT * 8 * 128 + (nt * 32 + lane) * 4);
-        float f1[2], f2[2];
-        const float m2[2] = {ml.x, ml.z}, l2[2] = {ml.y, ml.w};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float ms = fmaxf(mh[nt][e], m2[e]);
-          const float su = ms == -INFINITY ? 0.f : ms;
-          f1[e] = fast_exp2(mh[nt][e] - su);
-          f2[e] = fast_exp2(m2[e] - su);
-          lh[nt][e] = lh[nt][e] * f1[e] + l2[e] * f2[e];
-          mh[nt][e] = ms;
-        }
-#pragma unroll
-        for (int md = 0; md < 8; ++md) {
-          const float4 a = *reinterpret_cast<const float4*>(src + ((nt * 8 + md) * 32 + lane) * 4);
-          o[nt][md][0] = o[nt][md][0] * f1[0] + a.x * f2[0];
-          o[nt][md][1] = o[nt][md][1] * f1[1] + a.y * f2[1];
-          o[nt][md][2] = o[nt][md][2] * f1[0] + a.z * f2[0];
-          o[nt][md][3] = o[nt][md][3] * f1[1] + a.w * f2[1];
-        }
-      }
-    };
-    if (warp >= 2) hand_off(mw + (warp - 2) * wfl);
-    named_bar_sync(1, kCW * 32);
-    if (warp < 2) absorb(mw + warp * wfl);
-    named_bar_sync(1, kCW * 32);
-    if (warp == 1) hand_off(mw);
-    named_bar_sync(1, kCW * 32);
+    acc.merge_warps(mw, lay.merge_warp_bytes / 4, warp, lane);
     if (warp == 0) {
-      absorb(mw);
-      T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
       if (d.slot < 0) {
         // the item is this one chunk: its output row
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int hd0 = 8 * nt + 2 * tq;  // this thread's heads: hd0, hd0 + 1
-          const float i0 = 1.f / lh[nt][0], i1 = 1.f / lh[nt][1];
-#pragma unroll
-          for (int md = 0; md < 8; ++md) {
-            const int dd = 16 * md + gq;
-            if (hd0 < G) {
-              outg[(size_t)hd0 * kD + dd] = E::from_f(o[nt][md][0] * i0);
-              outg[(size_t)hd0 * kD + dd + 8] = E::from_f(o[nt][md][2] * i0);
-            }
-            if (hd0 + 1 < G) {
-              outg[(size_t)(hd0 + 1) * kD + dd] = E::from_f(o[nt][md][1] * i1);
-              outg[(size_t)(hd0 + 1) * kD + dd + 8] = E::from_f(o[nt][md][3] * i1);
-            }
-          }
-        }
+        acc.store_output(static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD, G, lane);
       } else {
         // this chunk's partial, then the item's arrival count
-        float* po = p.part_o + (size_t)d.slot * G * kD;
-        float* pm = p.part_ml + (size_t)d.slot * G * 2;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int hd0 = 8 * nt + 2 * tq;
-#pragma unroll
-          for (int md = 0; md < 8; ++md) {
-            const int dd = 16 * md + gq;
-            if (hd0 < G) {
-              po[(size_t)hd0 * kD + dd] = o[nt][md][0];
-              po[(size_t)hd0 * kD + dd + 8] = o[nt][md][2];
-            }
-            if (hd0 + 1 < G) {
-              po[(size_t)(hd0 + 1) * kD + dd] = o[nt][md][1];
-              po[(size_t)(hd0 + 1) * kD + dd + 8] = o[nt][md][3];
-            }
-          }
-          if (gq == 0) {
-            if (hd0 < G) *reinterpret_cast<float2*>(pm + 2 * hd0) = make_float2(mh[nt][0], lh[nt][0]);
-            if (hd0 + 1 < G) *reinterpret_cast<float2*>(pm + 2 * (hd0 + 1)) = make_float2(mh[nt][1], lh[nt][1]);
-          }
-        }
+        acc.store_partial(p.part_o + (size_t)d.slot * G * kD, p.part_ml + (size_t)d.slot * G * 2, G, lane);
         __syncwarp();  // (the merger's fence publishes the partial before counting it)
         if (lane == 0) {
           const int ms = mk % kMail;
