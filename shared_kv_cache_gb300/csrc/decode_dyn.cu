@@ -318,7 +318,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     decode_dyn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                       const DynParams p) {
   using E = Elem<T>;
-  constexpr bool kBF16 = E::is_bf16;
   const int G = p.G;
   const Layout lay = layout_for(G);
   extern __shared__ uint8_t smem_raw[];

@@ -166,8 +166,6 @@ template <typename T, int NT>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const DecodeParams p) {
-  using E = Elem<T>;
-  constexpr bool kBF16 = E::is_bf16;
   pdl_launch_dependents();
 
   const int G = p.G;

@@ -206,7 +206,7 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t ra
     CUtensorMapSwizzle swizzle;
     CUtensorMap map;
   };
-  constexpr int kEntries = 8;
+  constexpr int kEntries = 32;
   thread_local Entry cache[kEntries] = {};
   thread_local int next = 0;
   for (int e = 0; e < kEntries; ++e) {

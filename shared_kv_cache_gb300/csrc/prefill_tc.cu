@@ -65,8 +65,12 @@ constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKSt * kTileBytes;
 constexpr int kBiasHalfBytes = kBM * 64 * 2;  // bias block half: [128 query rows x 64 keys]
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain,
-// q_ready, bias_full[2], bias_empty[2]
-constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1 + 4;
+// q_ready, bias_full[2], bias_empty[2], cs_full
+constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1 + 4 + 1;
+// the rotary cos and sin rows of a query tile's 128 positions ([128 x 64],
+// 128-byte swizzled), loaded into V ring stage 1 before its first tile
+constexpr int kCosOff = kKOff + kKSt * kTileBytes + kTileBytes;
+constexpr int kSinOff = kCosOff + kBM * 128;
 // the kernels with a bias also hold the 2-stage bias ring (32 KB) after V
 template <bool kBias>
 struct SmemLayout {
@@ -110,6 +114,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
+
+// Bulk-tensor stores (TMA) from shared memory, tracked by the issuing
+// thread's bulk groups.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(w), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the committed stores have read their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Rotary embedding of query row `row` of a tile in shared memory: the
 // rotation of the append kernel (two pairs per packed instruction, the same
@@ -175,6 +197,8 @@ template <typename T, bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap bmap,
+                   const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap pmap,
+                   const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap smap,
                    const PrefillParams p) {
   using E = Elem<T>;
   using Lay = SmemLayout<kBias>;
@@ -193,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t q_ready = drain + 8;  // query tiles rotated in shared memory
   const uint32_t bias_full = q_ready + 8;      // [half 0, half 1]
   const uint32_t bias_empty = bias_full + 16;  // [half 0, half 1]
+  const uint32_t cs_full = bias_empty + 16;    // the cos / sin rows
   const bool rot = p.cos != nullptr;
   const bool bias_tma = kBias && p.bias_tma;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Lay::kSlotOff);
@@ -213,27 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pr = rem % p.n_pairs;
   const int hA = kh * p.G + 2 * pr;
   const bool has_b = 2 * pr + 1 < p.G;
-  const int past = p.seqlens[b];
-  if (sequence_error(past, p.S, p.M, p.total, p.evict)) return;  // recorded by the append kernel
   const int i0 = qt * kBM;
-  const int i1 = min(i0 + kBM, p.S);
-  const int L = past + p.S;
-  const int kstart = scan_start(past, i0, p.window);
-  const int kend = past + i1;  // one past the last key any row of the tile sees
-  // this CTA's share of the tile's keys: tiles [t_lo, t_lo + n_kv) of n_all
-  const int n_all = (kend - kstart + kBN - 1) / kBN;
-  const int ts = (n_all + p.n_split - 1) / p.n_split;
-  const int t_lo = sp * ts;
-  if (t_lo >= n_all) return;
-  const int n_kv = min(ts, n_all - t_lo);
-  const bool split = ts < n_all;  // partial results, merged by the combine kernel
-  const int kbase = kstart + t_lo * kBN;
-  // bf16 tiles whose first row sees few keys also carry P's rounding residue
-  // (P = hi + lo, both bf16; lo in the upper 64 columns of the S region) so
-  // that P.V keeps fp32-level accuracy where a few keys dominate the output
-  const int min_keys = p.window > 0 ? min(p.window, past + i0 + 1) : past + i0 + 1;
-  const bool splitp = kBF16 && min_keys <= 256;
 
+  // The barriers, and the query tiles' copy, go first: neither depends on
+  // the sequence's length, whose read would otherwise delay them.
   if (tid == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kKSt; ++s) {
@@ -255,7 +263,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bias_full + 8 * s, 1);
       mbar_init(bias_empty + 8 * s, 4 * (has_b ? 2 : 1));  // one arrival per softmax warp
     }
+    mbar_init(cs_full, 1);
     fence_mbar_init();
+    prefetch_tensormap(&qmap);
+    mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * kQBytes);
+    tma_load_4d(sb + kQOff, &qmap, 0, hA, i0, b, q_full);
+    tma_load_4d(sb + kQOff + kBoxBytes, &qmap, 64, hA, i0, b, q_full);
+    if (has_b) {
+      tma_load_4d(sb + kQOff + kQBytes, &qmap, 0, hA + 1, i0, b, q_full);
+      tma_load_4d(sb + kQOff + kQBytes + kBoxBytes, &qmap, 64, hA + 1, i0, b, q_full);
+    }
+  }
+  const int past = p.seqlens[b];
+  const int i1 = min(i0 + kBM, p.S);
+  const int L = past + p.S;
+  const int kstart = scan_start(past, i0, p.window);
+  const int kend = past + i1;  // one past the last key any row of the tile sees
+  // this CTA's share of the tile's keys: tiles [t_lo, t_lo + n_kv) of n_all
+  const int n_all = (kend - kstart + kBN - 1) / kBN;
+  const int ts = (n_all + p.n_split - 1) / p.n_split;
+  const int t_lo = sp * ts;
+  // (a length error is recorded by the append kernel); no work: leave once
+  // the query tiles' copy has landed
+  if (sequence_error(past, p.S, p.M, p.total, p.evict) || t_lo >= n_all) {
+    if (tid == 0) mbar_wait(q_full, 0, p.err);
+    return;
+  }
+  const int n_kv = min(ts, n_all - t_lo);
+  const bool split = ts < n_all;  // partial results, merged by the combine kernel
+  const int kbase = kstart + t_lo * kBN;
+  // bf16 tiles whose first row sees few keys also carry P's rounding residue
+  // (P = hi + lo, both bf16; lo in the upper 64 columns of the S region) so
+  // that P.V keeps fp32-level accuracy where a few keys dominate the output
+  const int min_keys = p.window > 0 ? min(p.window, past + i0 + 1) : past + i0 + 1;
+  const bool splitp = kBF16 && min_keys <= 256;
+  if (tid == 0 && rot) {
+    // the cos / sin rows of positions past + i0 .. + 127 (rows past the
+    // cache's end are filled with zeros and never used)
+    mbar_arrive_expect_tx(cs_full, 2 * kBM * 128);
+    tma_load_2d(sb + kCosOff, &cmap, 0, past + i0, cs_full);
+    tma_load_2d(sb + kSinOff, &smap, 0, past + i0, cs_full);
   }
   if (warp == 1) tc::alloc(smem_u32(tslot), kTmemCols);
   tc::fence_before();
@@ -268,17 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
       if (bias_tma) prefetch_tensormap(&bmap);
-      mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * kQBytes);
-      tma_load_4d(sb + kQOff, &qmap, 0, hA, i0, b, q_full);
-      tma_load_4d(sb + kQOff + kBoxBytes, &qmap, 64, hA, i0, b, q_full);
-      if (has_b) {
-        tma_load_4d(sb + kQOff + kQBytes, &qmap, 0, hA + 1, i0, b, q_full);
-        tma_load_4d(sb + kQOff + kQBytes + kBoxBytes, &qmap, 64, hA + 1, i0, b, q_full);
-      }
       const int zkv = b * p.Hkv + kh;
       const int zb = p.bias_h > 1 ? hA : 0, wb = p.bias_b > 1 ? b : 0;  // (one bias head when bias_tma)
       int issued_k = 0, issued_v = 0, issued_b = 0;
@@ -304,6 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (stop) break;
         }
         if (j >= kVSt && !mbar_wait(v_empty + 8 * vs, ((j / kVSt) - 1) & 1, p.err)) break;
+        // stage 1 holds the cos / sin rows until the query tiles are rotated
+        if (j == 1 && rot && !mbar_wait(q_ready, 0, p.err)) break;
         mbar_arrive_expect_tx(v_full + 8 * vs, kTileBytes);
         tma_load_3d(sb + kVOff + vs * kTileBytes, &vmap, 0, y, zkv, v_full + 8 * vs);
         tma_load_3d(sb + kVOff + vs * kTileBytes + kBoxBytes, &vmap, 64, y, zkv, v_full + 8 * vs);
@@ -311,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no copy may still be in flight into shared memory when the CTA exits
       mbar_wait(q_full, 0, p.err);
+      if (rot) mbar_wait(cs_full, 0, p.err);
       for (int j = max(0, issued_k - kKSt); j < issued_k; ++j)
         mbar_wait(k_full + 8 * (j % kKSt), (j / kKSt) & 1, p.err);
       for (int j = max(0, issued_v - kVSt); j < issued_v; ++j)
@@ -414,17 +456,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // sits in box j / 64, 16-byte chunk (j % 64) / 8, chunk slot
       // chunk ^ (row % 8)).  Rows past S hold the copy's zero fill.
       const bool do_row = active && i < p.S;
-      uint4 cq[8], sq[8];  // the position's cos and sin rows (64 values each)
-      if (do_row) {
-        const uint4* cr = reinterpret_cast<const uint4*>(static_cast<const T*>(p.cos) + (size_t)pos * (kD / 2));
-        const uint4* sr = reinterpret_cast<const uint4*>(static_cast<const T*>(p.sin) + (size_t)pos * (kD / 2));
+      const bool landed = mbar_wait(q_full, 0, p.err) && mbar_wait(cs_full, 0, p.err);
+      if (__all_sync(0xffffffffu, landed) && do_row) {
+        // the position's cos and sin rows (64 values each), 16-byte chunk c
+        // at slot c ^ (row % 8) of the swizzled rows
+        uint4 cq[8], sq[8];
+        const uint8_t* cr = smem + kCosOff + row * 128;
+        const uint8_t* sr = smem + kSinOff + row * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          cq[c] = cr[c];
-          sq[c] = sr[c];
+          cq[c] = *reinterpret_cast<const uint4*>(cr + ((c ^ (row & 7)) << 4));
+          sq[c] = *reinterpret_cast<const uint4*>(sr + ((c ^ (row & 7)) << 4));
         }
-      }
-      if (__all_sync(0xffffffffu, mbar_wait(q_full, 0, p.err)) && do_row) {
         rotate_query_row<T>(smem + kQOff + t * kQBytes + row * 128, row, cq, sq, p.interleaved != 0);
         fence_proxy_async_smem();  // visible to the tensor core's reads
       }
@@ -623,39 +666,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before();
       mbar_arrive(p_full + 8 * t);
     }
-    // epilogue: O / l to the output row, once every MMA has completed (the
-    // single-phase drain barrier; o_done could alias an older phase here)
+    // epilogue, once every MMA has completed (the single-phase drain barrier;
+    // o_done could alias an older phase here): O / l as 16-bit rows, or the
+    // key range's unnormalised fp32 O, staged in shared memory that no
+    // longer holds operands (the 128-byte-swizzled layout of the store
+    // boxes) and written by bulk-tensor stores; the output map clips rows
+    // past S
+    bool staged = false;
+    uint8_t* stg = split ? smem + (t == 0 ? kKOff : kVOff) : smem + kQOff + t * kQBytes;
+    const size_t prow0 = (((size_t)item * p.n_split + sp) * 2 + t) * kBM;
     if (ok && __all_sync(0xffffffffu, mbar_wait(drain, 0, p.err))) {
       tc::fence_after();
       const float inv = 1.f / l_run;
-      T* orow = static_cast<T*>(p.out) + ((size_t)(b * p.S + i) * p.H + h) * kD;
-      const size_t prow = (((size_t)item * p.n_split + sp) * 2 + t) * kBM + row;
       if (split && i < p.S)
-        *reinterpret_cast<float2*>(p.part_ml + prow * 2) = make_float2(m_ref, l_run);
+        *reinterpret_cast<float2*>(p.part_ml + (prow0 + row) * 2) = make_float2(m_ref, l_run);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tc::ld32(tO + c * 32, r);
         tc::wait_ld();
-        if (split && i < p.S) {
-          // unnormalised O of this key range, relative to m_ref
-          float4* po = reinterpret_cast<float4*>(p.part_o + prow * kD + c * 32);
+        if (split) {
+          // box c: columns 32c .. 32c + 31 of the 128 rows (128 bytes a row)
+          uint8_t* brow = stg + c * (kBM * 128) + row * 128;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            po[e / 4] = make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                                    __uint_as_float(r[e + 3]));
-        } else if (i < p.S) {
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(brow + ((q ^ (row & 7)) << 4)) =
+                make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        } else {
+          // 16-byte chunk cq = 4c + q of the row: box cq / 8, slot (cq % 8) ^ (row % 8)
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
+          for (int q = 0; q < 4; ++q) {
+            const int cq = 4 * c + q;
             uint4 v;
-            v.x = E::pack2(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv);
-            v.y = E::pack2(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv);
-            v.z = E::pack2(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv);
-            v.w = E::pack2(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+            v.x = E::pack2(__uint_as_float(r[8 * q]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+            v.y = E::pack2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+            v.z = E::pack2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+            v.w = E::pack2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+            *reinterpret_cast<uint4*>(stg + (cq >> 3) * kBoxBytes + row * 128 + (((cq & 7) ^ (row & 7)) << 4)) = v;
           }
         }
       }
+      fence_proxy_async_smem();  // visible to the bulk copies
+      staged = true;
+    }
+    // every thread of the warpgroup takes this barrier, whatever its waits
+    // gave; the stores go out only if all 128 rows were staged
+    if (named_bar_and(2 + t, 128, staged) && row == 0) {
+      if (split) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tma_store_2d(&pmap, smem_u32(stg) + c * (kBM * 128), 32 * c, (int)prow0);
+      } else {
+        tma_store_4d(&omap, smem_u32(stg), 0, h, i0, b);
+        tma_store_4d(&omap, smem_u32(stg) + kBoxBytes, 64, h, i0, b);
+      }
+      bulk_commit();
+      bulk_wait_read_all();  // shared memory stays valid until the CTA exits
     }
   }
   tc::fence_before();
@@ -774,6 +839,35 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   const int n_qt = (a.S + kBM - 1) / kBM;
   const int G = a.H / a.Hkv;
   const int n_pairs = (G + 1) / 2;
+  // the epilogue's stores: output rows [B, S, H, D] (token rows H * D
+  // elements apart) in [128 rows x 64] boxes, and the split partials as rows
+  // of 128 floats in [128 rows x 32] boxes
+  CUtensorMap omap, pmap{}, cmap{}, smap{};
+  if (a.cos) {
+    // positions 0 .. total - 1 are the ones a call can use
+    const cuuint64_t dims[2] = {(cuuint64_t)kD / 2, (cuuint64_t)a.total};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kBM};
+    if (!encode_tensor_map(&cmap, dt, 2, const_cast<void*>(a.cos), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map(&smap, dt, 2, const_cast<void*>(a.sin), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.S, (cuuint64_t)a.B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2, (cuuint64_t)a.S * a.H * kD * 2};
+    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
+    if (!encode_tensor_map(&omap, dt, 4, a.out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  if (n_split > 1) {
+    const cuuint64_t rows = prefill_split_rows(a.B, a.S, a.H, a.Hkv, n_split);
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 4};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kBM};
+    if (!encode_tensor_map(&pmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   PrefillParams p{};
   p.err = a.err;
   p.seqlens = a.seqlens;
@@ -808,7 +902,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
     if (e != cudaSuccess) return e;
   }
   const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
-  kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, p);
+  kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, omap, pmap, cmap, smap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
   // the split combine, overlapping the attention kernel's tail
