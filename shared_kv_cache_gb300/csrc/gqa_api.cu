@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "prefill_sched.cuh"
 
 namespace gqa {
 
@@ -162,10 +163,17 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
     // split the key ranges and need room for the partials
     pl.splits = prefill_splits(B, S, H, Hkv, total, num_sms);
     if (pl.splits > 1) {
+      // the length-aware work list: about 1.5 pieces per SM (fewer than
+      // target + items in all)
+      const long long items = (long long)B * Hkv * ((G + 1) / 2) * ((S + 127) / 128);
+      pl.sched_target = num_sms * 3 / 2;
+      pl.sched_cap = (int)std::min<long long>(items * pl.splits, pl.sched_target + items);
+      pl.sched_off = 0;
+      pl.sched_bytes = psched::bytes(pl.sched_cap, (int)items);
       const size_t rows = prefill_split_rows(B, S, H, Hkv, pl.splits);
-      pl.part_o_off = 0;
+      pl.part_o_off = align_up(pl.sched_bytes, 256);
       pl.part_o_bytes = rows * D * sizeof(float);
-      pl.part_ml_off = align_up(pl.part_o_bytes, 256);
+      pl.part_ml_off = align_up(pl.part_o_off + pl.part_o_bytes, 256);
       pl.part_ml_bytes = rows * 2 * sizeof(float);
       pl.total_bytes = align_up(pl.part_ml_off + pl.part_ml_bytes, 256);
     }
@@ -376,11 +384,13 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
     case Path::kGeneric: {
       void* q_rot = (cos_cache && pl.path == Path::kGeneric) ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
       void* k_new = evicting ? static_cast<void*>(ws + pl.k_new_off) : nullptr;
-      e = launch_rope_append(a, q_rot, k_new);
+      const PrefillSched ps{ws + pl.sched_off, pl.sched_cap, pl.sched_target, pl.splits};
+      const PrefillSched* psp = pl.path == Path::kPrefillTC && pl.sched_cap > 0 ? &ps : nullptr;
+      e = launch_rope_append(a, q_rot, k_new, psp);
       if (e == cudaSuccess)
         e = pl.path == Path::kPrefillTC
                 ? launch_prefill_tc(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
-                                    reinterpret_cast<float*>(ws + pl.part_ml_off))
+                                    reinterpret_cast<float*>(ws + pl.part_ml_off), psp)
                 : launch_attn_generic(a, q_rot ? q_rot : query, k_new);
       break;
     }

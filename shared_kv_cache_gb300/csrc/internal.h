@@ -58,7 +58,9 @@ struct Plan {
   size_t part_ml_off = 0, part_ml_bytes = 0;  // decode partial (max, sum), f32 [slots, G, 2]
   size_t sched_off = 0, sched_bytes = 0;      // decode chunk ticket + per-item arrival counters, u64 [1 + slots]
   int slots = 0;                              // decode partial slots
-  int splits = 1;                             // prefill: key-range splits per query tile
+  int splits = 1;                             // prefill: key-range splits per query tile (at most)
+  int sched_cap = 0;                          // split prefill: work-list capacity (the grid), 0: no list
+  int sched_target = 0;                       // split prefill: pieces the list aims at
   size_t total_bytes = 0;
 };
 
@@ -75,7 +77,16 @@ int device_smem_per_sm();
 // Rotary + append; with k_new set (evicting path) the rotated key rows go to
 // k_new [B, S, Hkv, D] instead of the buffer and the value rows are not
 // copied.
-cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new = nullptr);
+// With `sched` set (a split prefill), one extra CTA builds the prefill's
+// length-aware work list.
+struct PrefillSched {
+  void* base;  // workspace area of the list (prefill_sched.cuh layout)
+  int cap;     // list capacity: the prefill grid
+  int target;  // pieces the list aims at
+  int n_split; // pieces per work item at most
+};
+cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new = nullptr,
+                               const PrefillSched* sched = nullptr);
 // Evicting cache: keep the min(P_b + S, M) most recent tokens of every
 // (sequence, KV head) at slots [0, n_keep), new rows included (after the
 // step's attention has read the buffer).
@@ -97,7 +108,10 @@ int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
 // Tensor-core prefill; with n_split > 1 the key range of each query tile is
 // split and the partials (part_o: f32 [rows, D], part_ml: f32 [rows, 2], rows
 // from prefill_split_rows) are merged by a second kernel.
-cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml);
+// With `sched` set, CTA x takes the x-th piece of the work list built by the
+// append kernel (grid = sched->cap).
+cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
+                              const PrefillSched* sched = nullptr);
 int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms);
 size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split);
 

@@ -41,6 +41,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "prefill_sched.cuh"
 #include "tc.cuh"
 
 namespace gqa {
@@ -97,14 +98,12 @@ struct PrefillParams {
   float scale_log2;
   int evict;       // sliding-window cache: a full buffer is not an error (no call here evicts)
   int bias_tma;    // the bias blocks come through the shared-memory ring (bmap)
+  void* sched;     // length-aware work list (prefill_sched.cuh), or nullptr: CTA = work item x split
+  int sched_cap;   // its capacity (the grid)
 };
 
-// First key of a query tile's scan: the window start, rounded down to a
-// multiple of 8 so that every key tile starts on a 16-byte boundary of a bias
-// row (the keys before the window start are masked like any other).
-__host__ __device__ __forceinline__ int scan_start(int past, int i0, int window) {
-  return window > 0 ? (max(0, past + i0 - window + 1) & ~7) : 0;
-}
+using psched::scan_start;
+static_assert(psched::kQTile == kBM && psched::kKTile == kBN, "tile sizes");
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
                                             uint32_t bar) {
@@ -191,9 +190,10 @@ __device__ __forceinline__ void rotate_query_row(uint8_t* qrow, int row, const u
   }
 }
 
-// kBias: the call has an attention_bias (a separate instantiation, so that
-// calls without one carry no bias code)
-template <typename T, bool kBias>
+// kBias: the call has an attention_bias; kSched: CTAs take their work from
+// the length-aware list (separate instantiations, so that each kind of call
+// carries only its own code)
+template <typename T, bool kBias, bool kSched>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap bmap,
@@ -226,13 +226,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   pdl_launch_dependents();  // the split combine may be scheduled early
 
-  // work item: heaviest query tiles first; the split index is innermost
-  const int per_qt = p.B * p.Hkv * p.n_pairs * p.n_split;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x / per_qt);
-  const int rem_s = (int)(blockIdx.x % per_qt);
-  const int sp = rem_s % p.n_split;
-  const int rem = rem_s / p.n_split;
-  const int item = qt * (p.B * p.Hkv * p.n_pairs) + rem;
+  // work item: from the length-aware list (piece sp of k, key tiles
+  // [t_lo, t_lo + n_kv) of the scan), or heaviest query tiles first with the
+  // split index innermost
+  int item, sp, k_pieces = 0, t_lo_l = 0, n_l = 0, past_l = 0;
+  if constexpr (kSched) {
+    const int n_list = *psched::count_of(p.sched);
+    const int4 e = psched::list_of(p.sched)[blockIdx.x];
+    if ((int)blockIdx.x >= n_list) return;
+    item = e.x;
+    sp = e.y & 0xffff;
+    k_pieces = e.y >> 16;
+    t_lo_l = e.z & 0xffff;
+    n_l = e.z >> 16;
+    past_l = e.w;
+  } else {
+    const int per_qt = p.B * p.Hkv * p.n_pairs * p.n_split;
+    const int qt_s = p.n_qt - 1 - (int)(blockIdx.x / per_qt);
+    const int rem_s = (int)(blockIdx.x % per_qt);
+    sp = rem_s % p.n_split;
+    item = qt_s * (p.B * p.Hkv * p.n_pairs) + rem_s / p.n_split;
+  }
+  const int qt = item / (p.B * p.Hkv * p.n_pairs);
+  const int rem = item - qt * (p.B * p.Hkv * p.n_pairs);
   const int b = rem / (p.Hkv * p.n_pairs);
   const int kh = (rem / p.n_pairs) % p.Hkv;
   const int pr = rem % p.n_pairs;
@@ -274,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_4d(sb + kQOff + kQBytes + kBoxBytes, &qmap, 64, hA + 1, i0, b, q_full);
     }
   }
-  const int past = p.seqlens[b];
+  const int past = kSched ? past_l : p.seqlens[b];
   const int i1 = min(i0 + kBM, p.S);
   const int L = past + p.S;
   const int kstart = scan_start(past, i0, p.window);
@@ -282,15 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // this CTA's share of the tile's keys: tiles [t_lo, t_lo + n_kv) of n_all
   const int n_all = (kend - kstart + kBN - 1) / kBN;
   const int ts = (n_all + p.n_split - 1) / p.n_split;
-  const int t_lo = sp * ts;
-  // (a length error is recorded by the append kernel); no work: leave once
-  // the query tiles' copy has landed
-  if (sequence_error(past, p.S, p.M, p.total, p.evict) || t_lo >= n_all) {
+  const int t_lo = kSched ? t_lo_l : sp * ts;
+  // (a length error is recorded by the append kernel, and the list holds no
+  // piece of such a sequence); no work: leave once the query tiles' copy has
+  // landed
+  if (!kSched && (sequence_error(past, p.S, p.M, p.total, p.evict) || t_lo >= n_all)) {
     if (tid == 0) mbar_wait(q_full, 0, p.err);
     return;
   }
-  const int n_kv = min(ts, n_all - t_lo);
-  const bool split = ts < n_all;  // partial results, merged by the combine kernel
+  const int n_kv = kSched ? n_l : min(ts, n_all - t_lo);
+  // partial results, merged by the combine kernel
+  const bool split = kSched ? k_pieces > 1 : ts < n_all;
   const int kbase = kstart + t_lo * kBN;
   // bf16 tiles whose first row sees few keys also carry P's rounding residue
   // (P = hi + lo, both bf16; lo in the upper 64 columns of the S region) so
@@ -752,13 +770,18 @@ __global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParam
   pdl_wait_primary();
   if (!valid || sequence_error(past, p.S, p.M, p.total, p.evict)) return;
   const int qt = i / kBM, i0 = qt * kBM, i1 = min(i0 + kBM, p.S);
-  const int kstart = scan_start(past, i0, p.window);
-  const int n_all = (past + i1 - kstart + kBN - 1) / kBN;
-  const int ts = (n_all + p.n_split - 1) / p.n_split;
-  if (ts >= n_all) return;  // one key range: written directly
-  const int n_eff = (n_all + ts - 1) / ts;
   const int kh = h / p.G, gi = h - kh * p.G, pr = gi >> 1, t = gi & 1;
   const int item = qt * (p.B * p.Hkv * p.n_pairs) + (b * p.Hkv + kh) * p.n_pairs + pr;
+  int n_eff;  // key-range pieces of the row's item
+  if (p.sched) {
+    n_eff = psched::pieces_of(p.sched, p.sched_cap)[item];
+  } else {
+    const int kstart = scan_start(past, i0, p.window);
+    const int n_all = (past + i1 - kstart + kBN - 1) / kBN;
+    const int ts = (n_all + p.n_split - 1) / p.n_split;
+    n_eff = ts >= n_all ? 1 : (n_all + ts - 1) / ts;
+  }
+  if (n_eff <= 1) return;  // one key range: written directly
   const int row = i - i0;
   auto prow = [&](int s) { return (((size_t)item * p.n_split + s) * 2 + t) * kBM + row; };
   const int d4 = lane * 4;
@@ -802,8 +825,14 @@ __global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParam
   *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + ((size_t)(b * p.S + i) * p.H + h) * kD + d4) = packed;
 }
 
+#ifndef GQA_PREFILL_BIAS_RING
+#define GQA_PREFILL_BIAS_RING 1
+#endif
+constexpr bool kBiasRing = GQA_PREFILL_BIAS_RING != 0;  // one bias head: blocks through the shared-memory ring
+
 template <typename T>
-cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml) {
+cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
+                     const PrefillSched* ps) {
   const CUtensorMapDataType dt =
       a.dtype == GQA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap qmap, kmap, vmap;
@@ -826,7 +855,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   // the bias ring: one bias head for both heads of a CTA, rows of 16-byte
   // multiples at a 16-byte aligned base (the TMA's rules)
   CUtensorMap bmap{};
-  const bool bias_tma = a.bias && a.bias_h == 1 && a.total % 8 == 0 &&
+  const bool bias_tma = kBiasRing && a.bias && a.bias_h == 1 && a.total % 8 == 0 &&
                         (reinterpret_cast<uintptr_t>(a.bias) & 15) == 0;
   if (bias_tma) {
     const cuuint64_t dims[4] = {(cuuint64_t)a.total, (cuuint64_t)a.S, 1, (cuuint64_t)a.bias_b};
@@ -894,14 +923,18 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   p.scale_log2 = a.scale * kLog2e;
   p.evict = a.evict;
   p.bias_tma = bias_tma ? 1 : 0;
-  auto kern = a.bias ? prefill_kernel<T, true> : prefill_kernel<T, false>;
+  p.sched = ps ? ps->base : nullptr;
+  p.sched_cap = ps ? ps->cap : 0;
+  auto kern = a.bias ? (ps ? prefill_kernel<T, true, true> : prefill_kernel<T, true, false>)
+                     : (ps ? prefill_kernel<T, false, true> : prefill_kernel<T, false, false>);
   const int smem = a.bias ? SmemLayout<true>::kBytes : SmemLayout<false>::kBytes;
-  static std::atomic<int> smem_set[2][kMaxDevices];  // limit set so far, per instantiation and device
+  static std::atomic<int> smem_set[4][kMaxDevices];  // limit set so far, per instantiation and device
   {
-    const cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kern), smem, smem_set[a.bias ? 1 : 0]);
+    const cudaError_t e =
+        set_smem_limit(reinterpret_cast<const void*>(kern), smem, smem_set[(a.bias ? 2 : 0) + (ps ? 1 : 0)]);
     if (e != cudaSuccess) return e;
   }
-  const long long nblk = (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
+  const long long nblk = ps ? ps->cap : (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
   kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, omap, pmap, cmap, smap, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || n_split == 1) return e;
@@ -944,9 +977,10 @@ size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split) {
   return (size_t)B * Hkv * ((G + 1) / 2) * n_qt * n_split * 2 * kBM;
 }
 
-cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml) {
-  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src, n_split, part_o, part_ml)
-                                   : launch_t<__half>(a, q_src, n_split, part_o, part_ml);
+cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
+                              const PrefillSched* sched) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_src, n_split, part_o, part_ml, sched)
+                                   : launch_t<__half>(a, q_src, n_split, part_o, part_ml, sched);
 }
 
 }  // namespace gqa

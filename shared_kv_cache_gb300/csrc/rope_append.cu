@@ -12,6 +12,7 @@
 // (H + 2 Hkv) D elements plus one cos/sin row and writes the same amount.
 #include "common.cuh"
 #include "internal.h"
+#include "prefill_sched.cuh"
 
 namespace gqa {
 namespace {
@@ -31,6 +32,8 @@ struct RopeParams {
   int q_stride, kv_stride;  // elements between consecutive tokens' query / key and value rows
   void* k_new;              // evicting path: rotated key rows go here, [B, S, Hkv, D]; nullptr: to the buffer
   int evict;                // sliding-window cache: a full buffer is not an error
+  psched::Args sched;       // sched.base set: CTA 0 builds the split prefill's work list
+  int sched_cap;
 };
 
 template <typename T, int VEC>
@@ -76,7 +79,11 @@ __device__ __forceinline__ void rotate_vec(const T* src, T* dst, const T* cosr, 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
   using V = VecT<T, VEC>;
-  const int tok = blockIdx.x;
+  if (p.sched.base && blockIdx.x == 0) {
+    psched::build(p.sched, p.sched_cap);
+    return;
+  }
+  const int tok = blockIdx.x - (p.sched.base ? 1 : 0);
   const int b = tok / p.S;
   const int i = tok - b * p.S;
   const int past = p.seqlens[b];
@@ -133,10 +140,17 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
 }
 
 template <typename T>
-cudaError_t launch_t(const ForwardArgs& a, void* q_rot, void* k_new) {
+cudaError_t launch_t(const ForwardArgs& a, void* q_rot, void* k_new, const PrefillSched* ps) {
   RopeParams p{a.q, a.k, a.v, q_rot, a.kbuf, a.vbuf, a.seqlens, a.cos, a.sin, a.err,
-               a.S, a.H, a.Hkv, a.D, a.M, a.total, a.interleaved, a.q_stride, a.kv_stride, k_new, a.evict};
-  const dim3 grid(a.B * a.S);
+               a.S, a.H, a.Hkv, a.D, a.M, a.total, a.interleaved, a.q_stride, a.kv_stride, k_new, a.evict,
+               psched::Args{}, 0};
+  if (ps) {
+    const int G = a.H / a.Hkv;
+    p.sched = psched::Args{ps->base, a.seqlens, a.B, a.S, (a.S + psched::kQTile - 1) / psched::kQTile,
+                           a.Hkv * ((G + 1) / 2), a.window, a.M, a.total, a.evict, ps->n_split, ps->target};
+    p.sched_cap = ps->cap;
+  }
+  const dim3 grid(a.B * a.S + (ps ? 1 : 0));
   if ((a.D / 2) % 8 == 0)
     rope_append_kernel<T, 8><<<grid, 128, 0, a.stream>>>(p);
   else
@@ -146,8 +160,9 @@ cudaError_t launch_t(const ForwardArgs& a, void* q_rot, void* k_new) {
 
 }  // namespace
 
-cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new) {
-  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_rot, k_new) : launch_t<__half>(a, q_rot, k_new);
+cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new, const PrefillSched* sched) {
+  return a.dtype == GQA_DTYPE_BF16 ? launch_t<__nv_bfloat16>(a, q_rot, k_new, sched)
+                                   : launch_t<__half>(a, q_rot, k_new, sched);
 }
 
 }  // namespace gqa
