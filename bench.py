@@ -401,8 +401,7 @@ def cpu_baseline(name, min_seconds=10.0):
 # kernel per launch, from the ncu captures summarised in profiles/; a kernel
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
-    "decode_b16": 105392640 + 2887680,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
-    "prefill_2k": 109501952 + 30063360,    # prefill_kernel, profiles/prefill_kernel_prefill_2k.md
+    "decode_b16": 111428096 + 3087872,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
 }
 
 

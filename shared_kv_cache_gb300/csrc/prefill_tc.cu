@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // work item: from the length-aware list (piece sp of k, key tiles
   // [t_lo, t_lo + n_kv) of the scan), or heaviest query tiles first with the
   // split index innermost
-  int item, sp, k_pieces = 0, t_lo_l = 0, n_l = 0, past_l = 0;
+  int item, sp, qt, rem, k_pieces = 0, t_lo_l = 0, n_l = 0, past_l = 0;
   if constexpr (kSched) {
     const int n_list = *psched::count_of(p.sched);
     const int4 e = psched::list_of(p.sched)[blockIdx.x];
@@ -240,15 +240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     t_lo_l = e.z & 0xffff;
     n_l = e.z >> 16;
     past_l = e.w;
+    qt = item / (p.B * p.Hkv * p.n_pairs);
+    rem = item - qt * (p.B * p.Hkv * p.n_pairs);
   } else {
     const int per_qt = p.B * p.Hkv * p.n_pairs * p.n_split;
-    const int qt_s = p.n_qt - 1 - (int)(blockIdx.x / per_qt);
+    qt = p.n_qt - 1 - (int)(blockIdx.x / per_qt);
     const int rem_s = (int)(blockIdx.x % per_qt);
     sp = rem_s % p.n_split;
-    item = qt_s * (p.B * p.Hkv * p.n_pairs) + rem_s / p.n_split;
+    rem = rem_s / p.n_split;
+    item = qt * (p.B * p.Hkv * p.n_pairs) + rem;
   }
-  const int qt = item / (p.B * p.Hkv * p.n_pairs);
-  const int rem = item - qt * (p.B * p.Hkv * p.n_pairs);
   const int b = rem / (p.Hkv * p.n_pairs);
   const int kh = (rem / p.n_pairs) % p.Hkv;
   const int pr = rem % p.n_pairs;
