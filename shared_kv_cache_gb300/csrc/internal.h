@@ -105,9 +105,10 @@ int decode_ctas_per_sm(int group, int smem_per_sm);  // resident decode CTAs per
 // kernel (workspace laid out by make_plan; `epoch` is unique per call).
 cudaError_t launch_decode_dyn(const ForwardArgs& a, const Plan& plan, uint8_t* workspace, uint32_t epoch);
 int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
-// Tensor-core prefill; with n_split > 1 the key range of each query tile is
-// split and the partials (part_o: f32 [rows, D], part_ml: f32 [rows, 2], rows
-// from prefill_split_rows) are merged by a second kernel.
+// Tensor-core prefill; with n_split > 1 (and the work list) the key range of
+// each query tile may be split into up to n_split pieces, whose partials
+// (part_o: f32 [rows, D], part_ml: f32 [rows, 2], rows from
+// prefill_split_rows) the item's last piece merges.
 // With `sched` set, CTA x takes the x-th piece of the work list built by the
 // append kernel (grid = sched->cap).
 cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,

@@ -11,6 +11,8 @@
 // k = min(n_split, ceil(n / C)) contiguous pieces of ceil or floor of n / k
 // tiles.  The list holds fewer than target + items pieces (k < n / C + 1),
 // which bounds the grid.  One CTA builds it, from seqlens_k, on the device.
+// The pieces of an item leave fp32 partials; the item's last piece to finish
+// (its arrival count) merges them.
 #pragma once
 #include "common.cuh"
 
@@ -35,10 +37,11 @@ __host__ __device__ __forceinline__ int key_tiles(int past, int qt, int S, int w
 }
 
 // Workspace layout: a 16-byte header (int: number of pieces), `cap` entries
-// of 16 bytes, then one int per item (its number of pieces).
+// of 16 bytes, then one int per item (its number of pieces), then one int
+// per item (the arrival count of its pieces, zeroed by the builder).
 //   entry = {item, s | k << 16, t_lo | n << 16, past}
 // piece s of the item's k covers key tiles [t_lo, t_lo + n) of its scan.
-__host__ __device__ constexpr size_t bytes(int cap, int items) { return 16 + (size_t)cap * 16 + (size_t)items * 4; }
+__host__ __device__ constexpr size_t bytes(int cap, int items) { return 16 + (size_t)cap * 16 + (size_t)items * 8; }
 
 struct Args {
   void* base;  // the layout above
@@ -54,6 +57,7 @@ __device__ __forceinline__ int4* list_of(void* base) { return reinterpret_cast<i
 __device__ __forceinline__ int* pieces_of(void* base, int cap) {
   return reinterpret_cast<int*>(static_cast<uint8_t*>(base) + 16 + (size_t)cap * 16);
 }
+__device__ __forceinline__ int* arrivals_of(void* base, int cap, int items) { return pieces_of(base, cap) + items; }
 
 // Key tiles of class c = qt * B + b (0 for a sequence that fails the length
 // check: its error is recorded by the append kernel and it gets no piece).
@@ -125,12 +129,14 @@ __device__ inline void build(const Args& a, int cap) {
   int4* list = list_of(a.base);
   int* pieces = pieces_of(a.base, cap);
   const int items = classes * a.ipc;
+  int* arrivals = arrivals_of(a.base, cap, items);
   for (int it = tid; it < items; it += nthr) {
     const int c = it / a.ipc;
     int past;
     const int n = class_tiles(a, c, past);
     const int k = n == 0 ? 0 : min(a.n_split, (n + C - 1) / C);
     pieces[it] = k;
+    arrivals[it] = 0;
     if (k == 0) continue;
     const int q = n / k, r = n - q * k;
     for (int s = 0; s < k; ++s) {

@@ -35,6 +35,12 @@
 // ring that both softmax warpgroups read.  Otherwise (a bias per head, or
 // unaligned rows) the bias is added by a separate TMEM pass from global
 // loads.
+// A grid of fewer than two such items per SM takes its CTAs' work from a
+// length-aware list instead (prefill_sched.cuh): pieces of the items' key
+// ranges, longest first.  A piece of a split item writes its unnormalised O
+// and (m, l) in fp32; the item's last piece to finish merges them.
+// The epilogue stages each head's 128 rows in shared memory and writes them
+// with bulk-tensor stores.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 // With an odd group size the last head of each KV head runs alone (B idle).
 #include <type_traits>
@@ -66,8 +72,8 @@ constexpr int kKOff = kQOff + 2 * kQBytes;
 constexpr int kVOff = kKOff + kKSt * kTileBytes;
 constexpr int kBiasHalfBytes = kBM * 64 * 2;  // bias block half: [128 query rows x 64 keys]
 // barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], o_done[2], drain,
-// q_ready, bias_full[2], bias_empty[2], cs_full
-constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1 + 4 + 1;
+// q_ready, bias_full[2], bias_empty[2], cs_full, m_full[2]
+constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 2 + 1 + 1 + 4 + 1 + 2;
 // the rotary cos and sin rows of a query tile's 128 positions ([128 x 64],
 // 128-byte swizzled), loaded into V ring stage 1 before its first tile
 constexpr int kCosOff = kKOff + kKSt * kTileBytes + kTileBytes;
@@ -129,6 +135,8 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the committed stores have completed (their writes are performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // the committed stores have read their shared-memory sources
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
@@ -218,13 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bias_full = q_ready + 8;      // [half 0, half 1]
   const uint32_t bias_empty = bias_full + 16;  // [half 0, half 1]
   const uint32_t cs_full = bias_empty + 16;    // the cos / sin rows
+  const uint32_t m_full = cs_full + 8;         // [A, B]: another piece's partial, for the merge
   const bool rot = p.cos != nullptr;
   const bool bias_tma = kBias && p.bias_tma;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Lay::kSlotOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  pdl_launch_dependents();  // the split combine may be scheduled early
+  pdl_launch_dependents();  // a kernel launched after this one with PDL may be scheduled early
 
   // work item: from the length-aware list (piece sp of k, key tiles
   // [t_lo, t_lo + n_kv) of the scan), or heaviest query tiles first with the
@@ -281,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bias_empty + 8 * s, 4 * (has_b ? 2 : 1));  // one arrival per softmax warp
     }
     mbar_init(cs_full, 1);
+    mbar_init(m_full, 1);
+    mbar_init(m_full + 8, 1);
     fence_mbar_init();
     prefetch_tensormap(&qmap);
     mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * kQBytes);
@@ -308,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int n_kv = kSched ? n_l : min(ts, n_all - t_lo);
-  // partial results, merged by the combine kernel
-  const bool split = kSched ? k_pieces > 1 : ts < n_all;
+  // partial results, merged by the item's last piece
+  const bool split = kSched && k_pieces > 1;
   const int kbase = kstart + t_lo * kBN;
   // bf16 tiles whose first row sees few keys also carry P's rounding residue
   // (P = hi + lo, both bf16; lo in the upper 64 columns of the S region) so
@@ -730,16 +741,137 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // every thread of the warpgroup takes this barrier, whatever its waits
     // gave; the stores go out only if all 128 rows were staged
-    if (named_bar_and(2 + t, 128, staged) && row == 0) {
+    const bool all_staged = named_bar_and(2 + t, 128, staged);
+    if (all_staged && row == 0) {
       if (split) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tma_store_2d(&pmap, smem_u32(stg) + c * (kBM * 128), 32 * c, (int)prow0);
+        bulk_commit();
+        bulk_wait_all();  // the partial is in global memory before the item's count
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
       } else {
         tma_store_4d(&omap, smem_u32(stg), 0, h, i0, b);
         tma_store_4d(&omap, smem_u32(stg) + kBoxBytes, 64, h, i0, b);
+        bulk_commit();
+        bulk_wait_read_all();  // shared memory stays valid until the CTA exits
       }
-      bulk_commit();
-      bulk_wait_read_all();  // shared memory stays valid until the CTA exits
+    }
+    if constexpr (kSched) {
+      // A piece of a split item counts itself in once both heads' partials
+      // are written; the item's last piece merges the k partials of every
+      // row, m* = max m_s, o = sum 2^(m_s - m*) O_s / sum 2^(m_s - m*) l_s,
+      // and writes the output rows.
+      if (split) {
+        __threadfence();  // this thread's (m, l) store
+        const bool all_written = named_bar_and(4, 256, !active || all_staged);
+        int* flag = reinterpret_cast<int*>(tslot) + 1;
+        if (warp == 4 && lane == 0) {
+          int last = 0;
+          if (all_written) {
+            __threadfence();
+            int* arrive = psched::arrivals_of(p.sched, p.sched_cap, p.B * p.Hkv * p.n_pairs * p.n_qt);
+            last = atomicAdd(arrive + item, 1) == k_pieces - 1;
+            __threadfence();
+          }
+          *flag = last;
+        }
+        named_bar_sync(4, 256);
+        if (*flag && active) {
+          // The item's last piece: its own O is still in TMEM (relative to
+          // m_ref, sum l_run); every other piece's partial rows of this head
+          // come into the staging buffer by tensor copies, one piece at a
+          // time, and are added into TMEM with their weights 2^(m_s - m*).
+          const size_t prow_item = (size_t)item * p.n_split * 2 * kBM;  // piece s2: + (2 s2 + t) kBM
+          float ms = m_ref;
+          for (int s2 = 0; s2 < k_pieces; ++s2)
+            if (s2 != sp && i < p.S) ms = fmaxf(ms, __ldcg(p.part_ml + (prow_item + (size_t)(2 * s2 + t) * kBM + row) * 2));
+          const float mu = ms == -INFINITY ? 0.f : ms;
+          const float w_own = fast_exp2(m_ref - mu);
+          float lsum = l_run * w_own;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tc::ld32(tO + c * 32, r);
+            tc::wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * w_own);
+            tc::st32(tO + c * 32, r);
+          }
+          int nm = 0;  // partials merged (m_full phase)
+          bool mok = true;
+          for (int s2 = 0; s2 < k_pieces && mok; ++s2) {
+            if (s2 == sp) continue;
+            const size_t prow_s = prow_item + (size_t)(2 * s2 + t) * kBM;
+            if (row == 0) {
+              mbar_arrive_expect_tx(m_full + 8 * t, kBM * kD * 4);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                tma_load_2d(smem_u32(stg) + c * (kBM * 128), &pmap, 32 * c, (int)prow_s, m_full + 8 * t);
+            }
+            const float2 ml = i < p.S ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + (prow_s + row) * 2))
+                                      : make_float2(-INFINITY, 0.f);
+            const float w = fast_exp2(ml.x - mu);
+            lsum += w * ml.y;
+            mok = __all_sync(0xffffffffu, mbar_wait(m_full + 8 * t, nm & 1, p.err));
+            ++nm;
+            if (mok) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                uint32_t r[32];
+                tc::ld32(tO + c * 32, r);
+                tc::wait_ld();
+                const uint8_t* brow = stg + c * (kBM * 128) + row * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const float4 v = *reinterpret_cast<const float4*>(brow + ((q ^ (row & 7)) << 4));
+                  r[4 * q] = __float_as_uint(fmaf(w, v.x, __uint_as_float(r[4 * q])));
+                  r[4 * q + 1] = __float_as_uint(fmaf(w, v.y, __uint_as_float(r[4 * q + 1])));
+                  r[4 * q + 2] = __float_as_uint(fmaf(w, v.z, __uint_as_float(r[4 * q + 2])));
+                  r[4 * q + 3] = __float_as_uint(fmaf(w, v.w, __uint_as_float(r[4 * q + 3])));
+                }
+                tc::st32(tO + c * 32, r);
+              }
+              tc::wait_st();
+            }
+            // every thread has read the buffer before the next piece's copy
+            mok = named_bar_and(2 + t, 128, mok);
+          }
+          if (mok) {
+            // O / l as 16-bit rows, staged in the query tile's buffer
+            uint8_t* ostg = smem + kQOff + t * kQBytes;
+            const float inv = 1.f / lsum;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tc::ld32(tO + c * 32, r);
+              tc::wait_ld();
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int cq = 4 * c + q;
+                uint4 v;
+                v.x = E::pack2(__uint_as_float(r[8 * q]) * inv, __uint_as_float(r[8 * q + 1]) * inv);
+                v.y = E::pack2(__uint_as_float(r[8 * q + 2]) * inv, __uint_as_float(r[8 * q + 3]) * inv);
+                v.z = E::pack2(__uint_as_float(r[8 * q + 4]) * inv, __uint_as_float(r[8 * q + 5]) * inv);
+                v.w = E::pack2(__uint_as_float(r[8 * q + 6]) * inv, __uint_as_float(r[8 * q + 7]) * inv);
+                *reinterpret_cast<uint4*>(ostg + (cq >> 3) * kBoxBytes + row * 128 + (((cq & 7) ^ (row & 7)) << 4)) =
+                    v;
+              }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(2 + t, 128);
+            if (row == 0) {
+              tma_store_4d(&omap, smem_u32(ostg), 0, h, i0, b);
+              tma_store_4d(&omap, smem_u32(ostg) + kBoxBytes, 64, h, i0, b);
+              bulk_commit();
+              bulk_wait_read_all();
+            }
+          } else if (row == 0) {
+            // leave no copy in flight into shared memory
+            if (nm > 0) mbar_wait(m_full + 8 * t, (nm - 1) & 1, p.err);
+          }
+        }
+      }
     }
   }
   tc::fence_before();
@@ -748,82 +880,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after();
     tc::dealloc(tbase, kTmemCols);
   }
-}
-
-// Merges the key-range splits of the work items that were split: per output
-// row (b, i, h), with partials (O_s, m_s, l_s) of the splits s that had keys,
-//   m* = max m_s,  o = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s.
-// One warp per row, four dimensions per lane; the loads of up to kCombineBatch
-// splits are issued together (one round trip to L2 per batch).  Rows of
-// unsplit items were written by the attention kernel and are skipped.  The
-// lengths are read before waiting for the attention kernel (they are inputs).
-constexpr int kCombineBatch = 8;
-template <typename T>
-__global__ void __launch_bounds__(128) prefill_combine_kernel(const PrefillParams p) {
-  using E = Elem<T>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long r = (long long)blockIdx.x * 4 + warp;
-  const bool valid = r < (long long)p.B * p.S * p.H;
-  const int h = valid ? (int)(r % p.H) : 0;
-  const int i = valid ? (int)((r / p.H) % p.S) : 0;
-  const int b = valid ? (int)(r / ((long long)p.H * p.S)) : 0;
-  const int past = valid ? p.seqlens[b] : 0;
-  pdl_wait_primary();
-  if (!valid || sequence_error(past, p.S, p.M, p.total, p.evict)) return;
-  const int qt = i / kBM, i0 = qt * kBM, i1 = min(i0 + kBM, p.S);
-  const int kh = h / p.G, gi = h - kh * p.G, pr = gi >> 1, t = gi & 1;
-  const int item = qt * (p.B * p.Hkv * p.n_pairs) + (b * p.Hkv + kh) * p.n_pairs + pr;
-  int n_eff;  // key-range pieces of the row's item
-  if (p.sched) {
-    n_eff = psched::pieces_of(p.sched, p.sched_cap)[item];
-  } else {
-    const int kstart = scan_start(past, i0, p.window);
-    const int n_all = (past + i1 - kstart + kBN - 1) / kBN;
-    const int ts = (n_all + p.n_split - 1) / p.n_split;
-    n_eff = ts >= n_all ? 1 : (n_all + ts - 1) / ts;
-  }
-  if (n_eff <= 1) return;  // one key range: written directly
-  const int row = i - i0;
-  auto prow = [&](int s) { return (((size_t)item * p.n_split + s) * 2 + t) * kBM + row; };
-  const int d4 = lane * 4;
-  float m_run = -INFINITY, l = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < n_eff; s0 += kCombineBatch) {
-    float2 ml[kCombineBatch];
-    float4 o[kCombineBatch];
-#pragma unroll
-    for (int k = 0; k < kCombineBatch; ++k) {
-      const bool v = s0 + k < n_eff;
-      ml[k] = v ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + prow(s0 + k) * 2)) : make_float2(-INFINITY, 0.f);
-      o[k] = v ? __ldcg(reinterpret_cast<const float4*>(p.part_o + prow(s0 + k) * kD + d4))
-               : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float mb = m_run;
-#pragma unroll
-    for (int k = 0; k < kCombineBatch; ++k) mb = fmaxf(mb, ml[k].x);
-    const float base = mb == -INFINITY ? 0.f : mb;
-    const float sc = fast_exp2(m_run - base);  // 0 while nothing has been added
-    m_run = mb;
-    l *= sc;
-    acc.x *= sc;
-    acc.y *= sc;
-    acc.z *= sc;
-    acc.w *= sc;
-#pragma unroll
-    for (int k = 0; k < kCombineBatch; ++k) {
-      const float w = fast_exp2(ml[k].x - base);
-      l += w * ml[k].y;
-      acc.x += w * o[k].x;
-      acc.y += w * o[k].y;
-      acc.z += w * o[k].z;
-      acc.w += w * o[k].w;
-    }
-  }
-  const float inv = 1.f / l;
-  uint2 packed;
-  packed.x = E::pack2(acc.x * inv, acc.y * inv);
-  packed.y = E::pack2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + ((size_t)(b * p.S + i) * p.H + h) * kD + d4) = packed;
 }
 
 #ifndef GQA_PREFILL_BIAS_RING
@@ -937,19 +993,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   }
   const long long nblk = ps ? ps->cap : (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
   kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, omap, pmap, cmap, smap, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || n_split == 1) return e;
-  // the split combine, overlapping the attention kernel's tail
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(((long long)a.B * a.S * a.H + 3) / 4));
-  cfg.blockDim = dim3(128);
-  cfg.stream = a.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_combine_kernel<T>, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
