@@ -118,6 +118,11 @@ int* device_error_word() { return error_word_ptr(); }
 int device_sm_count() { return sm_count(); }
 int device_smem_per_sm() { return smem_per_sm(); }
 
+#ifndef GQA_PREFILL_PIECES_PER_SM2
+#define GQA_PREFILL_PIECES_PER_SM2 3
+#endif
+constexpr int kPrefillPiecesPerSm2 = GQA_PREFILL_PIECES_PER_SM2;  // split prefill: pieces aimed at per SM, x2
+
 Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms,
                bool evicting) {
   Plan pl{};
@@ -166,7 +171,7 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
       // the length-aware work list: about 1.5 pieces per SM (fewer than
       // target + items in all)
       const long long items = (long long)B * Hkv * ((G + 1) / 2) * ((S + 127) / 128);
-      pl.sched_target = num_sms * 3 / 2;
+      pl.sched_target = num_sms * kPrefillPiecesPerSm2 / 2;
       pl.sched_cap = (int)std::min<long long>(items * pl.splits, pl.sched_target + items);
       pl.sched_off = 0;
       pl.sched_bytes = psched::bytes(pl.sched_cap, (int)items);
@@ -174,7 +179,7 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
       pl.part_o_off = align_up(pl.sched_bytes, 256);
       pl.part_o_bytes = rows * D * sizeof(float);
       pl.part_ml_off = align_up(pl.part_o_off + pl.part_o_bytes, 256);
-      pl.part_ml_bytes = rows * 2 * sizeof(float);
+      pl.part_ml_bytes = rows * 4 * sizeof(float);
       pl.total_bytes = align_up(pl.part_ml_off + pl.part_ml_bytes, 256);
     }
     return pl;

@@ -107,7 +107,7 @@ cudaError_t launch_decode_dyn(const ForwardArgs& a, const Plan& plan, uint8_t* w
 int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
 // Tensor-core prefill; with n_split > 1 (and the work list) the key range of
 // each query tile may be split into up to n_split pieces, whose partials
-// (part_o: f32 [rows, D], part_ml: f32 [rows, 2], rows from
+// (part_o: f32 [rows, D], part_ml: f32 [rows, 4], rows from
 // prefill_split_rows) the item's last piece merges.
 // With `sched` set, CTA x takes the x-th piece of the work list built by the
 // append kernel (grid = sched->cap).

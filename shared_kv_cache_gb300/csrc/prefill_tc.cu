@@ -98,7 +98,7 @@ struct PrefillParams {
   const void* sin;
   void* out;  // [B, S, H*D]
   float* part_o;   // key-range splits: unnormalised O, [item][split][2][kBM][D]
-  float* part_ml;  // (reference max, sum) per row, [item][split][2][kBM][2]
+  float* part_ml;  // (reference max, sum, -, -) per row, [item][split][2][kBM][4]
   int B, S, H, Hkv, G, M, total, window, bias_b, bias_h, n_qt, n_pairs, interleaved;
   int n_split;     // key-range splits per work item (1: none)
   float scale_log2;
@@ -206,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap bmap,
                    const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap pmap,
-                   const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap smap,
-                   const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap mlmap, const __grid_constant__ CUtensorMap cmap,
+                   const __grid_constant__ CUtensorMap smap, const PrefillParams p) {
   using E = Elem<T>;
   using Lay = SmemLayout<kBias>;
   constexpr bool kBF16 = E::is_bf16;
@@ -708,8 +708,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && __all_sync(0xffffffffu, mbar_wait(drain, 0, p.err))) {
       tc::fence_after();
       const float inv = 1.f / l_run;
-      if (split && i < p.S)
-        *reinterpret_cast<float2*>(p.part_ml + (prow0 + row) * 2) = make_float2(m_ref, l_run);
+      if (split)  // (m, l) of the row, stored with the partial (the query buffer is free)
+        *reinterpret_cast<float4*>(smem + kQOff + t * kQBytes + row * 16) = make_float4(m_ref, l_run, 0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -746,10 +746,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (split) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) tma_store_2d(&pmap, smem_u32(stg) + c * (kBM * 128), 32 * c, (int)prow0);
+        tma_store_2d(&mlmap, smem_u32(smem + kQOff + t * kQBytes), 0, (int)prow0);
         bulk_commit();
         bulk_wait_all();  // the partial is in global memory before the item's count
         asm volatile("fence.proxy.async.global;" ::: "memory");
-        __threadfence();
       } else {
         tma_store_4d(&omap, smem_u32(stg), 0, h, i0, b);
         tma_store_4d(&omap, smem_u32(stg) + kBoxBytes, 64, h, i0, b);
@@ -763,16 +763,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row, m* = max m_s, o = sum 2^(m_s - m*) O_s / sum 2^(m_s - m*) l_s,
       // and writes the output rows.
       if (split) {
-        __threadfence();  // this thread's (m, l) store
         const bool all_written = named_bar_and(4, 256, !active || all_staged);
         int* flag = reinterpret_cast<int*>(tslot) + 1;
         if (warp == 4 && lane == 0) {
           int last = 0;
           if (all_written) {
-            __threadfence();
             int* arrive = psched::arrivals_of(p.sched, p.sched_cap, p.B * p.Hkv * p.n_pairs * p.n_qt);
-            last = atomicAdd(arrive + item, 1) == k_pieces - 1;
-            __threadfence();
+            int old;
+            // release: both heads' partials (completed bulk stores, ordered
+            // by the barrier) before the count; acquire: the other pieces'
+            // partials after it
+            asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(arrive + item) : "memory");
+            last = old == k_pieces - 1;
           }
           *flag = last;
         }
@@ -785,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const size_t prow_item = (size_t)item * p.n_split * 2 * kBM;  // piece s2: + (2 s2 + t) kBM
           float ms = m_ref;
           for (int s2 = 0; s2 < k_pieces; ++s2)
-            if (s2 != sp && i < p.S) ms = fmaxf(ms, __ldcg(p.part_ml + (prow_item + (size_t)(2 * s2 + t) * kBM + row) * 2));
+            if (s2 != sp && i < p.S) ms = fmaxf(ms, __ldcg(p.part_ml + (prow_item + (size_t)(2 * s2 + t) * kBM + row) * 4));
           const float mu = ms == -INFINITY ? 0.f : ms;
           const float w_own = fast_exp2(m_ref - mu);
           float lsum = l_run * w_own;
@@ -804,12 +806,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (s2 == sp) continue;
             const size_t prow_s = prow_item + (size_t)(2 * s2 + t) * kBM;
             if (row == 0) {
+              asm volatile("fence.proxy.async.global;" ::: "memory");  // the copies read what the count acquired
               mbar_arrive_expect_tx(m_full + 8 * t, kBM * kD * 4);
 #pragma unroll
               for (int c = 0; c < 4; ++c)
                 tma_load_2d(smem_u32(stg) + c * (kBM * 128), &pmap, 32 * c, (int)prow_s, m_full + 8 * t);
             }
-            const float2 ml = i < p.S ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + (prow_s + row) * 2))
+            const float2 ml = i < p.S ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + (prow_s + row) * 4))
                                       : make_float2(-INFINITY, 0.f);
             const float w = fast_exp2(ml.x - mu);
             lsum += w * ml.y;
@@ -928,7 +931,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
   // the epilogue's stores: output rows [B, S, H, D] (token rows H * D
   // elements apart) in [128 rows x 64] boxes, and the split partials as rows
   // of 128 floats in [128 rows x 32] boxes
-  CUtensorMap omap, pmap{}, cmap{}, smap{};
+  CUtensorMap omap, pmap{}, mlmap{}, cmap{}, smap{};
   if (a.cos) {
     // positions 0 .. total - 1 are the ones a call can use
     const cuuint64_t dims[2] = {(cuuint64_t)kD / 2, (cuuint64_t)a.total};
@@ -952,6 +955,13 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
     const cuuint32_t box[2] = {32, (cuuint32_t)kBM};
     if (!encode_tensor_map(&pmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_o, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    // (m, l, -, -) rows of 16 bytes
+    const cuuint64_t mdims[2] = {4, rows};
+    const cuuint64_t mstrides[1] = {16};
+    const cuuint32_t mbox[2] = {4, (cuuint32_t)kBM};
+    if (!encode_tensor_map(&mlmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, part_ml, mdims, mstrides, mbox,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
   PrefillParams p{};
@@ -992,7 +1002,7 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
     if (e != cudaSuccess) return e;
   }
   const long long nblk = ps ? ps->cap : (long long)a.B * a.Hkv * n_pairs * n_qt * n_split;
-  kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, omap, pmap, cmap, smap, p);
+  kern<<<(unsigned)nblk, kThreads, smem, a.stream>>>(qmap, kmap, vmap, bmap, omap, pmap, mlmap, cmap, smap, p);
   return cudaGetLastError();
 }
 

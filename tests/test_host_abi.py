@@ -195,8 +195,8 @@ def test_workspace_plan_prefill_splits():
     assert gqa.gqa_workspace_size(big, 2048, 0) == 0
     # a smaller grid cuts each query tile's key range into at most
     # min(ceil(3 * 152 / CTAs), key tiles + 1) pieces and keeps fp32 partials
-    # (rows = CTAs x pieces x 2 query tiles x 128 rows; D floats plus (m, l)
-    # each), after the work list: a 16-byte header, one 16-byte entry per
+    # (rows = CTAs x pieces x 2 query tiles x 128 rows; D floats plus a
+    # 16-byte (m, l) record each), after the work list: a 16-byte header, one 16-byte entry per
     # CTA of the grid (min(items x pieces, 1.5 x 152 + items)) and two ints
     # per item (its piece count and arrival count)
     small = dims(batch=8, seq_len=128, num_heads=32, kv_num_heads=8, head_size=128, max_seq_len=4096)
@@ -205,7 +205,7 @@ def test_workspace_plan_prefill_splits():
     assert pieces == 4
     rows = ctas * pieces * 2 * 128
     sched = _r256(16 + min(ctas * pieces, 152 * 3 // 2 + ctas) * 16 + ctas * 8)
-    assert gqa.gqa_workspace_size(small, 4096, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 2 * 4)
+    assert gqa.gqa_workspace_size(small, 4096, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 4 * 4)
     # few key tiles bound the pieces
     short = dims(batch=1, seq_len=128, num_heads=8, kv_num_heads=8, head_size=128, max_seq_len=4096)
     ctas = 1 * 8 * 1 * 1
@@ -213,7 +213,7 @@ def test_workspace_plan_prefill_splits():
     assert pieces == 3
     rows = ctas * pieces * 2 * 128
     sched = _r256(16 + min(ctas * pieces, 152 * 3 // 2 + ctas) * 16 + ctas * 8)
-    assert gqa.gqa_workspace_size(short, 256, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 2 * 4)
+    assert gqa.gqa_workspace_size(short, 256, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 4 * 4)
 
 
 def test_workspace_plan_decode_large_group():
