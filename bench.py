@@ -402,6 +402,8 @@ def cpu_baseline(name, min_seconds=10.0):
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
     "decode_b16": 111428096 + 3087872,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
+    "prefill_2k": 112835328 + 33319936,    # prefill_kernel, profiles/prefill_kernel_prefill_2k.md
+    "chunked_prefill": 67845888 + 4827392,  # prefill_kernel, profiles/prefill_kernel_chunked_prefill.md
 }
 
 
