@@ -269,10 +269,10 @@ __device__ __forceinline__ ChunkDesc chunk_in_block(const DynParams& p, const Pa
 }
 
 // Batches of at most 32 sequences: the partition and chunk u (u < 0: none)
-// in one warp pass.
-__device__ ChunkDesc partition_and_locate_small(const DynParams& p, const int* sl, int u, int lane, Partition& pt) {
+// in one warp pass; `len` is sequence lane's seqlens_k entry.
+__device__ ChunkDesc partition_and_locate_small(const DynParams& p, int len, int u, int lane, Partition& pt) {
   int lo = 0, L = 0;
-  const int tb = lane < p.B ? seq_tiles(p, sl[lane], lo, L) : 0;
+  const int tb = lane < p.B ? seq_tiles(p, len, lo, L) : 0;
   const int T = warp_sum(tb) * p.Hkv;
   const int target = chunk_target(p, T);
   pt.C = max(2, (T + target - 1) / target);
@@ -355,22 +355,58 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   pdl_launch_dependents();
-  // While the previous kernel in the stream may still run: warm L2 with the
-  // lengths and with K/V tiles this call will read.  An L2 prefetch only
-  // moves lines into L2, which the previous kernel's writes update, so it
-  // reads nothing before the dependency wait below.  Without a window every
-  // item's keys start at 0: CTA c asks for item c % items, tiles
-  // [kPrefetchTiles * (c / items), ...) (a tile beyond an item's length is
-  // fetched for nothing).
-  if (warp == kProducer && lane == 0) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.seqlens) : "memory");
-    if (p.window == 0 && !p.evicting) {
-      const int items = p.B * p.Hkv;
-      const int item = c % items, t0 = (c / items) * kPrefetchTiles;
-      for (int t = t0; t < t0 + kPrefetchTiles && (t + 1) * kTile <= p.M; ++t) {
-        const size_t off = ((size_t)item * p.M + (size_t)t * kTile) * kD;
-        bulk_prefetch_l2(static_cast<const T*>(p.kbuf) + off, kTile * kD * 2);
-        bulk_prefetch_l2(static_cast<const T*>(p.vbuf) + off, kTile * kD * 2);
+  // While the previous kernel in the stream may still run: warm L2 with
+  // what this call will read first.  An L2 prefetch only moves lines into
+  // L2, which the previous kernel's writes update, so it reads nothing before
+  // the dependency wait below.
+  // - Without a window every item's keys start at 0: CTA c asks at once for
+  //   item c % items, tiles [kPrefetchTiles * (c / items), ...) (a tile
+  //   beyond an item's length is fetched for nothing).
+  // - Batches of at most 32 sequences also take a speculative look at
+  //   seqlens_k (through L2, never L1).  The partition and this CTA's first
+  //   chunk computed from it give the chunk's query, cos and sin rows to
+  //   prefetch, and with a window (where the guess above does not apply) its
+  //   first tiles.  Both are kept if the lengths read after the wait are the
+  //   same.  (The exact tiles on top of the guess were slower on the batched
+  //   decode: the extra prefetches compete with the previous call's tail.)
+  int spec_len = 0;
+  Partition spec_pt{};
+  ChunkDesc spec_first{};
+  spec_first.u = -1;
+  if (warp == kProducer) {
+    const bool guess = p.window == 0 && !p.evicting;
+    if (lane == 0) {
+      if (p.B > 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.seqlens) : "memory");
+      if (guess) {
+        const int items = p.B * p.Hkv;
+        const int item = c % items, t0 = (c / items) * kPrefetchTiles;
+        for (int t = t0; t < t0 + kPrefetchTiles && (t + 1) * kTile <= p.M; ++t) {
+          const size_t off = ((size_t)item * p.M + (size_t)t * kTile) * kD;
+          bulk_prefetch_l2(static_cast<const T*>(p.kbuf) + off, kTile * kD * 2);
+          bulk_prefetch_l2(static_cast<const T*>(p.vbuf) + off, kTile * kD * 2);
+        }
+      }
+    }
+    if (p.B <= 32) {
+      spec_len = lane < p.B ? __ldcg(p.seqlens + lane) : 0;
+      spec_first = partition_and_locate_small(p, spec_len, c, lane, spec_pt);
+      if (lane == 0 && spec_first.u >= 0) {
+        const ChunkDesc& d = spec_first;
+        if (!guess) {
+          const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo - (p.evicting ? slot0_position(d.L - 1, p.M) : 0);
+          for (int t = d.t0; t < min(d.t1, d.t0 + kPrefetchTiles); ++t) {
+            const size_t off = ((size_t)row0 + (size_t)t * kTile) * kD;
+            bulk_prefetch_l2(static_cast<const T*>(p.kbuf) + off, kTile * kD * 2);
+            bulk_prefetch_l2(static_cast<const T*>(p.vbuf) + off, kTile * kD * 2);
+          }
+        }
+        bulk_prefetch_l2(static_cast<const T*>(p.q) + (size_t)d.b * p.q_stride + (size_t)d.kh * G * kD, G * kD * 2);
+        if (p.cos) {
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const T*>(p.cos) + (size_t)(d.L - 1) * (kD / 2))
+                       : "memory");
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const T*>(p.sin) + (size_t)(d.L - 1) * (kD / 2))
+                       : "memory");
+        }
       }
     }
   }
@@ -382,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int* s_seq = reinterpret_cast<int*>(smem + lay.seq_off);
     const bool cached = p.B <= kSeqCache;
     if (cached)
-      for (int i = lane; i < p.B; i += 32) s_seq[i] = p.seqlens[i];
+      for (int i = lane; i < p.B; i += 32) s_seq[i] = __ldcg(p.seqlens + i);
     __syncwarp();
     const int* sl = cached ? s_seq : p.seqlens;
     if (c == 0)  // sequences that fail the length check are skipped and reported once
@@ -393,7 +429,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     Partition pt;
     ChunkDesc first{};
     if (p.B <= 32) {
-      first = partition_and_locate_small(p, sl, c, lane, pt);
+      const int len = lane < p.B ? sl[lane] : 0;
+      if (__all_sync(0xffffffffu, len == spec_len)) {
+        first = spec_first;  // the lengths did not change across the wait
+        pt = spec_pt;
+      } else {
+        first = partition_and_locate_small(p, len, c, lane, pt);
+      }
     } else {
       pt = make_partition(p, sl, lane);
       first.u = -1;

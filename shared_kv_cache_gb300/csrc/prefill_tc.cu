@@ -783,57 +783,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The item's last piece: its own O is still in TMEM (relative to
           // m_ref, sum l_run); every other piece's partial rows of this head
           // come into the staging buffer by tensor copies, one piece at a
-          // time, and are added into TMEM with their weights 2^(m_s - m*).
+          // time.  The sum o = sum_s 2^(m_s - m*) O_s runs in piece order
+          // whichever piece is last (the same rounding every call), in the
+          // head's S columns of TMEM, free since the drain.
           const size_t prow_item = (size_t)item * p.n_split * 2 * kBM;  // piece s2: + (2 s2 + t) kBM
           float ms = m_ref;
           for (int s2 = 0; s2 < k_pieces; ++s2)
             if (s2 != sp && i < p.S) ms = fmaxf(ms, __ldcg(p.part_ml + (prow_item + (size_t)(2 * s2 + t) * kBM + row) * 4));
           const float mu = ms == -INFINITY ? 0.f : ms;
-          const float w_own = fast_exp2(m_ref - mu);
-          float lsum = l_run * w_own;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tc::ld32(tO + c * 32, r);
-            tc::wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * w_own);
-            tc::st32(tO + c * 32, r);
-          }
-          int nm = 0;  // partials merged (m_full phase)
+          float lsum = 0.f;
+          int nm = 0;  // partials copied (m_full phase)
           bool mok = true;
           for (int s2 = 0; s2 < k_pieces && mok; ++s2) {
-            if (s2 == sp) continue;
+            const bool own = s2 == sp;
             const size_t prow_s = prow_item + (size_t)(2 * s2 + t) * kBM;
-            if (row == 0) {
-              asm volatile("fence.proxy.async.global;" ::: "memory");  // the copies read what the count acquired
-              mbar_arrive_expect_tx(m_full + 8 * t, kBM * kD * 4);
+            float w, l;
+            if (own) {
+              w = fast_exp2(m_ref - mu);
+              l = l_run;
+            } else {
+              if (row == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");  // the copies read what the count acquired
+                mbar_arrive_expect_tx(m_full + 8 * t, kBM * kD * 4);
 #pragma unroll
-              for (int c = 0; c < 4; ++c)
-                tma_load_2d(smem_u32(stg) + c * (kBM * 128), &pmap, 32 * c, (int)prow_s, m_full + 8 * t);
+                for (int c = 0; c < 4; ++c)
+                  tma_load_2d(smem_u32(stg) + c * (kBM * 128), &pmap, 32 * c, (int)prow_s, m_full + 8 * t);
+              }
+              const float2 ml = i < p.S ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + (prow_s + row) * 4))
+                                        : make_float2(-INFINITY, 0.f);
+              w = fast_exp2(ml.x - mu);
+              l = ml.y;
+              mok = __all_sync(0xffffffffu, mbar_wait(m_full + 8 * t, nm & 1, p.err));
+              ++nm;
             }
-            const float2 ml = i < p.S ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + (prow_s + row) * 4))
-                                      : make_float2(-INFINITY, 0.f);
-            const float w = fast_exp2(ml.x - mu);
-            lsum += w * ml.y;
-            mok = __all_sync(0xffffffffu, mbar_wait(m_full + 8 * t, nm & 1, p.err));
-            ++nm;
+            lsum = fmaf(w, l, lsum);
             if (mok) {
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tc::ld32(tO + c * 32, r);
+                uint32_t acc[32], v[32];
+                if (s2 > 0) tc::ld32(tS + c * 32, acc);
+                if (own) tc::ld32(tO + c * 32, v);
                 tc::wait_ld();
-                const uint8_t* brow = stg + c * (kBM * 128) + row * 128;
+                if (!own) {
+                  const uint8_t* brow = stg + c * (kBM * 128) + row * 128;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                  const float4 v = *reinterpret_cast<const float4*>(brow + ((q ^ (row & 7)) << 4));
-                  r[4 * q] = __float_as_uint(fmaf(w, v.x, __uint_as_float(r[4 * q])));
-                  r[4 * q + 1] = __float_as_uint(fmaf(w, v.y, __uint_as_float(r[4 * q + 1])));
-                  r[4 * q + 2] = __float_as_uint(fmaf(w, v.z, __uint_as_float(r[4 * q + 2])));
-                  r[4 * q + 3] = __float_as_uint(fmaf(w, v.w, __uint_as_float(r[4 * q + 3])));
+                  for (int q = 0; q < 8; ++q) {
+                    const float4 f = *reinterpret_cast<const float4*>(brow + ((q ^ (row & 7)) << 4));
+                    v[4 * q] = __float_as_uint(f.x);
+                    v[4 * q + 1] = __float_as_uint(f.y);
+                    v[4 * q + 2] = __float_as_uint(f.z);
+                    v[4 * q + 3] = __float_as_uint(f.w);
+                  }
                 }
-                tc::st32(tO + c * 32, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  acc[e] = __float_as_uint(fmaf(w, __uint_as_float(v[e]), s2 > 0 ? __uint_as_float(acc[e]) : 0.f));
+                tc::st32(tS + c * 32, acc);
               }
               tc::wait_st();
             }
@@ -847,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
               uint32_t r[32];
-              tc::ld32(tO + c * 32, r);
+              tc::ld32(tS + c * 32, r);
               tc::wait_ld();
 #pragma unroll
               for (int q = 0; q < 4; ++q) {

@@ -148,3 +148,16 @@ def test_evicting_mode_without_overflow_uses_the_plain_path():
     st, dst, out, kb, vb = run_cuda(bad)
     assert st == gqa.GQA_OK and dst == gqa.GQA_ERR_INVALID_ARGUMENT
     assert torch.isnan(out[1].float()).all()
+
+
+# ---------------------------------------------------------------------------
+# Determinism of the split prefill
+# ---------------------------------------------------------------------------
+def test_split_prefill_gives_the_same_bits_every_call():
+    """The chunked prefill's items are cut into pieces whose partials the
+    item's last piece merges; which piece is last varies from call to call,
+    the merged output must not."""
+    inp = W.make_inputs(W.CONFIGS["chunked_prefill"])
+    outs = [W.bits(run_cuda(inp)[2]) for _ in range(4)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
