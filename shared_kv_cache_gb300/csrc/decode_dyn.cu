@@ -216,11 +216,21 @@ __device__ __forceinline__ int chunk_target(const DynParams& p, int T) {
   return T <= kShortTilesPerCta * p.P ? p.P : p.chunks_per_cta * p.P;
 }
 
-// The partition, computed identically by every producer warp: per-sequence
-// tile counts, the chunk size C and the chunk count U.
+// The partition, computed identically by every producer warp: the chunk
+// size C, and each item's chunks in two groups -- its whole chunks of C
+// tiles, then (when C does not divide its tiles) one shorter remainder chunk.
+// Chunks are numbered all whole chunks first, then all remainders, so the
+// chunks handed out last by the ticket are the short ones and the CTAs'
+// end times stay close.  An item of n >= 2 chunks keeps n partial slots,
+// whole chunks first.
 struct Partition {
-  int C, U;
+  int C;
+  int UA, U;  // whole chunks; all chunks
 };
+__device__ __forceinline__ void item_chunks(int C, int tb, int& nA, int& nB) {
+  nA = tb / C;
+  nB = tb - nA * C > 0 ? 1 : 0;
+}
 __device__ Partition make_partition(const DynParams& p, const int* sl, int lane) {
   int T = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
@@ -230,24 +240,28 @@ __device__ Partition make_partition(const DynParams& p, const int* sl, int lane)
   }
   T *= p.Hkv;
   const int target = chunk_target(p, T);
-  const int C = max(2, (T + target - 1) / target);
-  int U = 0;
+  Partition pt{max(2, (T + target - 1) / target), 0, 0};
+  int UA = 0, UB = 0;
   for (int b0 = 0; b0 < p.B; b0 += 32) {
-    int lo, L;
+    int lo, L, nA, nB;
     const int b = b0 + lane;
-    const int tb = b < p.B ? seq_tiles(p, sl[b], lo, L) : 0;
-    U += warp_sum((tb + C - 1) / C);
+    item_chunks(pt.C, b < p.B ? seq_tiles(p, sl[b], lo, L) : 0, nA, nB);
+    UA += warp_sum(nA);
+    UB += warp_sum(nB);
   }
-  return Partition{C, U * p.Hkv};
+  pt.UA = UA * p.Hkv;
+  pt.U = (UA + UB) * p.Hkv;
+  return pt;
 }
 
-// Chunk u within one block of 32 sequences b0 + lane, given each lane's tile
-// count, key range and the block's inclusive scans of chunks (incl) and
-// partial slots (sincl); cbase / sbase count those of earlier blocks.
-__device__ __forceinline__ ChunkDesc chunk_in_block(const DynParams& p, const Partition& pt, int u, int b0, int tb,
-                                                    int lo, int L, int nb, int ch, int sl_n, int incl, int sincl,
-                                                    int cbase, int sbase) {
-  const unsigned m = __ballot_sync(0xffffffffu, cbase + incl > u);
+// Chunk u within one block of 32 sequences b0 + lane.  Each lane brings its
+// sequence's tile count, key range and chunk counts; incl / sincl are the
+// block's inclusive scans of this group's chunks and of partial slots, cbase
+// / sbase those of earlier blocks; v counts chunks within the group.
+__device__ __forceinline__ ChunkDesc chunk_in_block(const DynParams& p, const Partition& pt, int u, int v, bool rem,
+                                                    int b0, int tb, int lo, int L, int nA, int nB, int ch, int sl_n,
+                                                    int incl, int sincl, int cbase, int sbase) {
+  const unsigned m = __ballot_sync(0xffffffffu, cbase + incl > v);
   const int l = __ffs(m) - 1;
   ChunkDesc d;
   d.b = b0 + l;
@@ -256,15 +270,17 @@ __device__ __forceinline__ ChunkDesc chunk_in_block(const DynParams& p, const Pa
   d.tb = __shfl_sync(0xffffffffu, tb, l);
   d.klo = __shfl_sync(0xffffffffu, lo, l);
   d.L = __shfl_sync(0xffffffffu, L, l);
-  d.n = __shfl_sync(0xffffffffu, nb, l);
-  const int r = u - c0;
-  d.kh = r / d.n;
-  const int k = r - d.kh * d.n;
-  d.t0 = k * pt.C;
-  d.t1 = min(d.t0 + pt.C, d.tb);
+  const int na = __shfl_sync(0xffffffffu, nA, l), nb = __shfl_sync(0xffffffffu, nB, l);
+  d.n = na + nb;
+  const int np = rem ? nb : na;  // this group's chunks of each of the sequence's items
+  const int r = v - c0;
+  d.kh = r / np;
+  const int k = r - d.kh * np;
+  d.t0 = rem ? na * pt.C : k * pt.C;
+  d.t1 = rem ? d.tb : d.t0 + pt.C;
   d.u = u;
   d.first_slot = d.n > 1 ? s0 + d.kh * d.n : -1;
-  d.slot = d.n > 1 ? d.first_slot + k : -1;
+  d.slot = d.n > 1 ? d.first_slot + (rem ? na : k) : -1;
   return d;
 }
 
@@ -276,35 +292,41 @@ __device__ ChunkDesc partition_and_locate_small(const DynParams& p, int len, int
   const int T = warp_sum(tb) * p.Hkv;
   const int target = chunk_target(p, T);
   pt.C = max(2, (T + target - 1) / target);
-  const int nb = (tb + pt.C - 1) / pt.C;
-  const int ch = nb * p.Hkv;
-  const int sl_n = nb > 1 ? ch : 0;
-  const int incl = warp_incl_scan(ch, lane);
-  const int sincl = warp_incl_scan(sl_n, lane);
-  pt.U = __shfl_sync(0xffffffffu, incl, 31);
+  int nA, nB;
+  item_chunks(pt.C, tb, nA, nB);
+  pt.UA = warp_sum(nA) * p.Hkv;
+  pt.U = pt.UA + warp_sum(nB) * p.Hkv;
   if (u < 0 || u >= pt.U) {
     ChunkDesc d{};
     d.u = -1;
     return d;
   }
-  return chunk_in_block(p, pt, u, 0, tb, lo, L, nb, ch, sl_n, incl, sincl, 0, 0);
+  const bool rem = u >= pt.UA;
+  const int v = rem ? u - pt.UA : u;
+  const int ch = (rem ? nB : nA) * p.Hkv;
+  const int sl_n = nA + nB > 1 ? (nA + nB) * p.Hkv : 0;
+  const int incl = warp_incl_scan(ch, lane);
+  const int sincl = warp_incl_scan(sl_n, lane);
+  return chunk_in_block(p, pt, u, v, rem, 0, tb, lo, L, nA, nB, ch, sl_n, incl, sincl, 0, 0);
 }
 
 // Warp-cooperative: the item and tile range of chunk u (< U).
 __device__ ChunkDesc locate_chunk(const DynParams& p, const int* sl, const Partition& pt, int u, int lane) {
-  int cbase = 0, sbase = 0;  // chunks and partial slots of the sequences before b0
+  const bool rem = u >= pt.UA;
+  const int v = rem ? u - pt.UA : u;
+  int cbase = 0, sbase = 0;  // this group's chunks and partial slots of the sequences before b0
   for (int b0 = 0; b0 < p.B; b0 += 32) {
-    int lo, L;
+    int lo, L, nA, nB;
     const int b = b0 + lane;
     const int tb = b < p.B ? seq_tiles(p, sl[b], lo, L) : 0;
-    const int nb = (tb + pt.C - 1) / pt.C;
-    const int ch = nb * p.Hkv;
-    const int sl_n = nb > 1 ? ch : 0;
+    item_chunks(pt.C, tb, nA, nB);
+    const int ch = (rem ? nB : nA) * p.Hkv;
+    const int sl_n = nA + nB > 1 ? (nA + nB) * p.Hkv : 0;
     const int incl = warp_incl_scan(ch, lane);
     const int sincl = warp_incl_scan(sl_n, lane);
     const int chunk_total = __shfl_sync(0xffffffffu, incl, 31);
-    if (u < cbase + chunk_total)
-      return chunk_in_block(p, pt, u, b0, tb, lo, L, nb, ch, sl_n, incl, sincl, cbase, sbase);
+    if (v < cbase + chunk_total)
+      return chunk_in_block(p, pt, u, v, rem, b0, tb, lo, L, nA, nB, ch, sl_n, incl, sincl, cbase, sbase);
     cbase += chunk_total;
     sbase += __shfl_sync(0xffffffffu, sincl, 31);
   }
