@@ -73,7 +73,10 @@ constexpr int kSeqCache = 128;               // seqlens_k entries cached in shar
 #define GQA_PREFETCH_TILES 4
 #endif
 constexpr int kPrefetchTiles = GQA_PREFETCH_TILES;            // K/V tiles per CTA asked of L2 before the lengths are known
-constexpr int kShortTilesPerCta = 24;        // see chunk_target
+#ifndef GQA_DECODE_SHORT_TILES
+#define GQA_DECODE_SHORT_TILES 24
+#endif
+constexpr int kShortTilesPerCta = GQA_DECODE_SHORT_TILES;  // see chunk_target
 constexpr int kMergeBatch = 4;               // partials loaded per round of a merge (registers)
 
 // Descriptor of one chunk, written by the producer into a staging slot.

@@ -61,6 +61,7 @@ struct Plan {
   int splits = 1;                             // prefill: key-range splits per query tile (at most)
   int sched_cap = 0;                          // split prefill: work-list capacity (the grid), 0: no list
   int sched_target = 0;                       // split prefill: pieces the list aims at
+  int sched_ipc = 0;                          // split prefill: work items per (sequence, query tile)
   size_t total_bytes = 0;
 };
 
@@ -84,6 +85,8 @@ struct PrefillSched {
   int cap;     // list capacity: the prefill grid
   int target;  // pieces the list aims at
   int n_split; // pieces per work item at most
+  int ipc;     // work items per (sequence, query tile)
+  int ktile;   // keys per key tile of the prefill kernel
 };
 cudaError_t launch_rope_append(const ForwardArgs& a, void* q_rot, void* k_new = nullptr,
                                const PrefillSched* sched = nullptr);
@@ -114,6 +117,13 @@ int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
 cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
                               const PrefillSched* sched = nullptr);
 int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms);
+// Tensor-core prefill with one query head per CTA and two CTAs per SM
+// (64-key tiles; the query tile in TMEM); the work list and split partials
+// as above, per (sequence, head, query tile) item.
+cudaError_t launch_prefill_head(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
+                                const PrefillSched* sched = nullptr);
+int prefill_head_splits(int B, int S, int H, int total, int num_sms);
+size_t prefill_head_split_rows(int B, int S, int H, int n_split);
 size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split);
 
 // Staging copies of up to kMaxStageSegs byte ranges (each a multiple of 4

@@ -19,8 +19,7 @@
 namespace gqa {
 namespace psched {
 
-constexpr int kQTile = 128;    // query rows per tile (the prefill kernel's tile)
-constexpr int kKTile = 128;    // keys per key tile
+constexpr int kQTile = 128;    // query rows per tile (the prefill kernels' tile)
 constexpr int kBuckets = 1024;  // piece sizes sorted exactly up to 1023 tiles
 
 // First key of a query tile's scan: the window start, rounded down to a
@@ -30,10 +29,11 @@ __host__ __device__ __forceinline__ int scan_start(int past, int i0, int window)
   return window > 0 ? (max(0, past + i0 - window + 1) & ~7) : 0;
 }
 
-// Key tiles that query tile qt of a sequence with `past` earlier tokens scans.
-__host__ __device__ __forceinline__ int key_tiles(int past, int qt, int S, int window) {
+// Key tiles of `ktile` keys that query tile qt of a sequence with `past`
+// earlier tokens scans.
+__host__ __device__ __forceinline__ int key_tiles(int past, int qt, int S, int window, int ktile) {
   const int i0 = qt * kQTile, i1 = min(i0 + kQTile, S);
-  return (past + i1 - scan_start(past, i0, window) + kKTile - 1) / kKTile;
+  return (past + i1 - scan_start(past, i0, window) + ktile - 1) / ktile;
 }
 
 // Workspace layout: a 16-byte header (int: number of pieces), `cap` entries
@@ -50,6 +50,7 @@ struct Args {
   int window, M, total, evict;
   int n_split;  // pieces per item at most
   int target;   // pieces aimed at
+  int ktile;    // keys per key tile of the prefill kernel
 };
 
 __device__ __forceinline__ int* count_of(void* base) { return static_cast<int*>(base); }
@@ -64,7 +65,7 @@ __device__ __forceinline__ int* arrivals_of(void* base, int cap, int items) { re
 __device__ __forceinline__ int class_tiles(const Args& a, int c, int& past) {
   const int b = c % a.B, qt = c / a.B;
   past = a.seqlens[b];
-  return sequence_error(past, a.S, a.M, a.total, a.evict) ? 0 : key_tiles(past, qt, a.S, a.window);
+  return sequence_error(past, a.S, a.M, a.total, a.evict) ? 0 : key_tiles(past, qt, a.S, a.window, a.ktile);
 }
 
 // Built by every thread of one CTA (any block size that is a multiple of 32,

@@ -109,7 +109,7 @@ struct PrefillParams {
 };
 
 using psched::scan_start;
-static_assert(psched::kQTile == kBM && psched::kKTile == kBN, "tile sizes");
+static_assert(psched::kQTile == kBM, "tile sizes");
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
                                             uint32_t bar) {

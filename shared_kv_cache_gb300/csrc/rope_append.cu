@@ -145,9 +145,8 @@ cudaError_t launch_t(const ForwardArgs& a, void* q_rot, void* k_new, const Prefi
                a.S, a.H, a.Hkv, a.D, a.M, a.total, a.interleaved, a.q_stride, a.kv_stride, k_new, a.evict,
                psched::Args{}, 0};
   if (ps) {
-    const int G = a.H / a.Hkv;
     p.sched = psched::Args{ps->base, a.seqlens, a.B, a.S, (a.S + psched::kQTile - 1) / psched::kQTile,
-                           a.Hkv * ((G + 1) / 2), a.window, a.M, a.total, a.evict, ps->n_split, ps->target};
+                           ps->ipc, a.window, a.M, a.total, a.evict, ps->n_split, ps->target, ps->ktile};
     p.sched_cap = ps->cap;
   }
   const dim3 grid(a.B * a.S + (ps ? 1 : 0));

@@ -189,30 +189,31 @@ def test_workspace_plan_generic_path():
 
 
 def test_workspace_plan_prefill_splits():
-    # tensor-core prefill: a grid of at least two CTAs per SM (B * Hkv *
-    # ceil(G / 2) * query tiles >= 2 * 152) needs no scratch
+    # tensor-core prefill, one query head per CTA and two CTAs per SM: a grid
+    # of at least two CTAs per CTA slot (B * H * query tiles >= 2 * 2 * 152)
+    # needs no scratch
     big = dims(batch=4, seq_len=2048, num_heads=32, kv_num_heads=8, head_size=128, max_seq_len=4096)
     assert gqa.gqa_workspace_size(big, 2048, 0) == 0
-    # a smaller grid cuts each query tile's key range into at most
-    # min(ceil(3 * 152 / CTAs), key tiles + 1) pieces and keeps fp32 partials
-    # (rows = CTAs x pieces x 2 query tiles x 128 rows; D floats plus a
-    # 16-byte (m, l) record each), after the work list: a 16-byte header, one 16-byte entry per
-    # CTA of the grid (min(items x pieces, 1.5 x 152 + items)) and two ints
-    # per item (its piece count and arrival count)
+    # a smaller grid cuts each item's key range into at most
+    # max(2, min(ceil(3 * 304 / items), 64-key tiles + 1)) pieces and keeps
+    # fp32 partials (rows = items x pieces x 128 rows; D floats plus a
+    # 16-byte (m, l) record each), after the work list: a 16-byte header, one
+    # 16-byte entry per CTA of the grid (min(items x pieces, 1.5 x 304 +
+    # items)) and two ints per item (its piece count and arrival count)
     small = dims(batch=8, seq_len=128, num_heads=32, kv_num_heads=8, head_size=128, max_seq_len=4096)
-    ctas = 8 * 8 * 2 * 1
-    pieces = min(-(-3 * 152 // ctas), 4096 // 128 + 1)
+    items = 8 * 32 * 1
+    pieces = min(-(-3 * 304 // items), 4096 // 64 + 1)
     assert pieces == 4
-    rows = ctas * pieces * 2 * 128
-    sched = _r256(16 + min(ctas * pieces, 152 * 3 // 2 + ctas) * 16 + ctas * 8)
+    rows = items * pieces * 128
+    sched = _r256(16 + min(items * pieces, 304 * 3 // 2 + items) * 16 + items * 8)
     assert gqa.gqa_workspace_size(small, 4096, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 4 * 4)
     # few key tiles bound the pieces
     short = dims(batch=1, seq_len=128, num_heads=8, kv_num_heads=8, head_size=128, max_seq_len=4096)
-    ctas = 1 * 8 * 1 * 1
-    pieces = min(-(-3 * 152 // ctas), 256 // 128 + 1)
-    assert pieces == 3
-    rows = ctas * pieces * 2 * 128
-    sched = _r256(16 + min(ctas * pieces, 152 * 3 // 2 + ctas) * 16 + ctas * 8)
+    items = 1 * 8 * 1
+    pieces = min(-(-3 * 304 // items), 256 // 64 + 1)
+    assert pieces == 5
+    rows = items * pieces * 128
+    sched = _r256(16 + min(items * pieces, 304 * 3 // 2 + items) * 16 + items * 8)
     assert gqa.gqa_workspace_size(short, 256, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 4 * 4)
 
 
