@@ -119,13 +119,9 @@ int device_sm_count() { return sm_count(); }
 int device_smem_per_sm() { return smem_per_sm(); }
 
 #ifndef GQA_PREFILL_PIECES_PER_SM2
-#define GQA_PREFILL_PIECES_PER_SM2 3
+#define GQA_PREFILL_PIECES_PER_SM2 4
 #endif
-#ifndef GQA_PREFILL_HEAD
-#define GQA_PREFILL_HEAD 1
-#endif
-constexpr bool kPrefillHead = GQA_PREFILL_HEAD != 0;  // prefill: one head per CTA, two CTAs per SM
-constexpr int kPrefillPiecesPerSm2 = GQA_PREFILL_PIECES_PER_SM2;  // split prefill: pieces aimed at per SM, x2
+constexpr int kPrefillPiecesPerSm2 = GQA_PREFILL_PIECES_PER_SM2;  // split prefill: pieces aimed at per CTA slot, x2
 
 Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool rotary, int num_sms,
                bool evicting) {
@@ -170,19 +166,17 @@ Plan make_plan(int B, int S, int H, int Hkv, int D, int total, int window, bool 
   if (pl.path == Path::kPrefillTC) {
     // the tensor-core prefill rotates its query tiles itself; small grids
     // split the key ranges and need room for the partials
-    pl.splits = kPrefillHead ? prefill_head_splits(B, S, H, total, num_sms)
-                             : prefill_splits(B, S, H, Hkv, total, num_sms);
+    pl.splits = prefill_head_splits(B, S, H, total, num_sms);
     if (pl.splits > 1) {
-      // the length-aware work list: about 1.5 pieces per CTA slot (fewer
+      // the length-aware work list: about 2 pieces per CTA slot (fewer
       // than target + items in all)
-      pl.sched_ipc = kPrefillHead ? H : Hkv * ((G + 1) / 2);
+      pl.sched_ipc = H;
       const long long items = (long long)B * pl.sched_ipc * ((S + 127) / 128);
-      pl.sched_target = num_sms * (kPrefillHead ? 2 : 1) * kPrefillPiecesPerSm2 / 2;
+      pl.sched_target = num_sms * 2 * kPrefillPiecesPerSm2 / 2;
       pl.sched_cap = (int)std::min<long long>(items * pl.splits, pl.sched_target + items);
       pl.sched_off = 0;
       pl.sched_bytes = psched::bytes(pl.sched_cap, (int)items);
-      const size_t rows = kPrefillHead ? prefill_head_split_rows(B, S, H, pl.splits)
-                                       : prefill_split_rows(B, S, H, Hkv, pl.splits);
+      const size_t rows = prefill_head_split_rows(B, S, H, pl.splits);
       pl.part_o_off = align_up(pl.sched_bytes, 256);
       pl.part_o_bytes = rows * D * sizeof(float);
       pl.part_ml_off = align_up(pl.part_o_off + pl.part_o_bytes, 256);
@@ -397,15 +391,13 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
       void* q_rot = (cos_cache && pl.path == Path::kGeneric) ? static_cast<void*>(ws + pl.q_rot_off) : nullptr;
       void* k_new = evicting ? static_cast<void*>(ws + pl.k_new_off) : nullptr;
       const PrefillSched ps{ws + pl.sched_off, pl.sched_cap, pl.sched_target, pl.splits, pl.sched_ipc,
-                            kPrefillHead ? 64 : 128};
+                            kPrefillKeyTile};
       const PrefillSched* psp = pl.path == Path::kPrefillTC && pl.sched_cap > 0 ? &ps : nullptr;
       e = launch_rope_append(a, q_rot, k_new, psp);
       if (e == cudaSuccess)
         e = pl.path == Path::kPrefillTC
-                ? (kPrefillHead ? launch_prefill_head(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
-                                                      reinterpret_cast<float*>(ws + pl.part_ml_off), psp)
-                                : launch_prefill_tc(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
-                                                    reinterpret_cast<float*>(ws + pl.part_ml_off), psp))
+                ? launch_prefill_head(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
+                                      reinterpret_cast<float*>(ws + pl.part_ml_off), psp)
                 : launch_attn_generic(a, q_rot ? q_rot : query, k_new);
       break;
     }

@@ -108,23 +108,17 @@ int decode_ctas_per_sm(int group, int smem_per_sm);  // resident decode CTAs per
 // kernel (workspace laid out by make_plan; `epoch` is unique per call).
 cudaError_t launch_decode_dyn(const ForwardArgs& a, const Plan& plan, uint8_t* workspace, uint32_t epoch);
 int decode_dyn_ctas_per_sm(int group, int smem_per_sm);
-// Tensor-core prefill; with n_split > 1 (and the work list) the key range of
-// each query tile may be split into up to n_split pieces, whose partials
-// (part_o: f32 [rows, D], part_ml: f32 [rows, 4], rows from
-// prefill_split_rows) the item's last piece merges.
-// With `sched` set, CTA x takes the x-th piece of the work list built by the
-// append kernel (grid = sched->cap).
-cudaError_t launch_prefill_tc(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
-                              const PrefillSched* sched = nullptr);
-int prefill_splits(int B, int S, int H, int Hkv, int total, int num_sms);
 // Tensor-core prefill with one query head per CTA and two CTAs per SM
-// (64-key tiles; the query tile in TMEM); the work list and split partials
-// as above, per (sequence, head, query tile) item.
+// (64-key tiles, double-buffered S in TMEM).  With n_split > 1 (and the work
+// list) the key range of each (sequence, head, query tile) item may be split
+// into up to n_split pieces, whose partials (part_o: f32 [rows, D], part_ml:
+// f32 [rows, 4], rows from prefill_head_split_rows) the item's last piece
+// merges.
+constexpr int kPrefillKeyTile = 64;  // keys per K/V tile of the prefill kernel
 cudaError_t launch_prefill_head(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
                                 const PrefillSched* sched = nullptr);
 int prefill_head_splits(int B, int S, int H, int total, int num_sms);
 size_t prefill_head_split_rows(int B, int S, int H, int n_split);
-size_t prefill_split_rows(int B, int S, int H, int Hkv, int n_split);
 
 // Staging copies of up to kMaxStageSegs byte ranges (each a multiple of 4
 // bytes at 4-byte aligned addresses; either side may be page-locked host

@@ -70,7 +70,7 @@ constexpr int kBarOff = kVOff + kVSt * kTileBytes;
 constexpr int kSlotOff = kBarOff + kNumBars * 8;
 constexpr int kSmemBytes = kSlotOff + 16 + 1024;
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
-static_assert(psched::kQTile == kBM, "query tile");
+static_assert(psched::kQTile == kBM && kPrefillKeyTile == kBN, "tile sizes");
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 0, kColS = 128;  // S buffer s at kColS + 64 s
 constexpr float kRescaleThresh = 8.0f;  // log2 units: rescale O only when the max grows by > 2^8
@@ -883,6 +883,11 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
 
 }  // namespace
 
+#ifndef GQA_PREFILL_SPLIT_FACTOR
+#define GQA_PREFILL_SPLIT_FACTOR 3
+#endif
+constexpr int kSplitFactor = GQA_PREFILL_SPLIT_FACTOR;  // pieces per CTA slot at most, over all items
+
 int prefill_head_splits(int B, int S, int H, int total, int num_sms) {
   // A grid of fewer than two CTAs per CTA slot (two per SM) takes the
   // length-aware list, with at most kSplitFactor * slots / items pieces per
@@ -892,7 +897,7 @@ int prefill_head_splits(int B, int S, int H, int total, int num_sms) {
   const long long slots = 2ll * num_sms;
   if (base >= 2 * slots) return 1;
   const int max_tiles = (total + kBN - 1) / kBN + 1;
-  const long long want = (3 * slots + base - 1) / base;
+  const long long want = (kSplitFactor * slots + base - 1) / base;
   return want < 2 ? 2 : (int)(want > max_tiles ? max_tiles : want);
 }
 size_t prefill_head_split_rows(int B, int S, int H, int n_split) {

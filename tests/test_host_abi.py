@@ -198,14 +198,14 @@ def test_workspace_plan_prefill_splits():
     # max(2, min(ceil(3 * 304 / items), 64-key tiles + 1)) pieces and keeps
     # fp32 partials (rows = items x pieces x 128 rows; D floats plus a
     # 16-byte (m, l) record each), after the work list: a 16-byte header, one
-    # 16-byte entry per CTA of the grid (min(items x pieces, 1.5 x 304 +
+    # 16-byte entry per CTA of the grid (min(items x pieces, 2 x 304 +
     # items)) and two ints per item (its piece count and arrival count)
     small = dims(batch=8, seq_len=128, num_heads=32, kv_num_heads=8, head_size=128, max_seq_len=4096)
     items = 8 * 32 * 1
     pieces = min(-(-3 * 304 // items), 4096 // 64 + 1)
     assert pieces == 4
     rows = items * pieces * 128
-    sched = _r256(16 + min(items * pieces, 304 * 3 // 2 + items) * 16 + items * 8)
+    sched = _r256(16 + min(items * pieces, 304 * 2 + items) * 16 + items * 8)
     assert gqa.gqa_workspace_size(small, 4096, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 4 * 4)
     # few key tiles bound the pieces
     short = dims(batch=1, seq_len=128, num_heads=8, kv_num_heads=8, head_size=128, max_seq_len=4096)
@@ -213,7 +213,7 @@ def test_workspace_plan_prefill_splits():
     pieces = min(-(-3 * 304 // items), 256 // 64 + 1)
     assert pieces == 5
     rows = items * pieces * 128
-    sched = _r256(16 + min(items * pieces, 304 * 3 // 2 + items) * 16 + items * 8)
+    sched = _r256(16 + min(items * pieces, 304 * 2 + items) * 16 + items * 8)
     assert gqa.gqa_workspace_size(short, 256, 0) == _r256(sched + _r256(rows * 128 * 4) + rows * 4 * 4)
 
 
