@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // [t_lo, t_lo + n_kv) of the scan), or heaviest query tiles first
   int item, sp = 0, k_pieces = 1, t_lo_l = 0, n_l = 0, past_l = 0, qt, rem;
   if constexpr (kSched) {
+    pdl_wait_primary();  // the list is the append kernel's
     const int n_list = *psched::count_of(p.sched);
     const int4 e = psched::list_of(p.sched)[blockIdx.x];
     if ((int)blockIdx.x >= n_list) return;
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) {
         prefetch_tensormap(&kmap);
         prefetch_tensormap(&vmap);
+        pdl_wait_primary();  // the new K/V rows are the append kernel's
         const int zkv = b * p.Hkv + kh;
         int issued_k = 0, issued_v = 0;
         for (int j = 0; j < n_kv; ++j) {
@@ -877,8 +879,22 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src, int n_split, float
     if (e != cudaSuccess) return e;
   }
   const long long nblk = ps ? ps->cap : (long long)a.B * a.H * n_qt;
-  kern<<<(unsigned)nblk, kThreads, kSmemBytes, a.stream>>>(qmap, kmap, vmap, omap, pmap, mlmap, cmap, smap, p);
-  return cudaGetLastError();
+  // Launched with programmatic dependent launch: the CTAs' prologue (query
+  // tile, cos/sin rows, rotation, TMEM) overlaps the append kernel, and the
+  // producer waits for it (griddepcontrol.wait) before the first K/V copy.
+  // (A call with the work list reads the list the append kernel builds, so
+  // its CTAs wait at once.)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)nblk);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, qmap, kmap, vmap, omap, pmap, mlmap, cmap, smap, p);
 }
 
 }  // namespace

@@ -79,6 +79,10 @@ __device__ __forceinline__ void rotate_vec(const T* src, T* dst, const T* cosr, 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
   using V = VecT<T, VEC>;
+  // the attention kernel after this one (programmatic dependent launch)
+  // may start its own prologue; it waits for this grid before it reads the
+  // buffer
+  pdl_launch_dependents();
   if (p.sched.base && blockIdx.x == 0) {
     psched::build(p.sched, p.sched_cap);
     return;
