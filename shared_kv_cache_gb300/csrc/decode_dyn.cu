@@ -73,6 +73,14 @@ constexpr int kSeqCache = 128;               // seqlens_k entries cached in shar
 #define GQA_PREFETCH_TILES 4
 #endif
 constexpr int kPrefetchTiles = GQA_PREFETCH_TILES;            // K/V tiles per CTA asked of L2 before the lengths are known
+#ifndef GQA_DECODE_GUESS_TILES
+#define GQA_DECODE_GUESS_TILES GQA_PREFETCH_TILES
+#endif
+#ifndef GQA_DECODE_EXACT_TILES
+#define GQA_DECODE_EXACT_TILES 0
+#endif
+constexpr int kGuessTiles = GQA_DECODE_GUESS_TILES;  // without a window: guessed tiles per CTA
+constexpr int kExactTiles = GQA_DECODE_EXACT_TILES;  // ... and the first chunk's first tiles
 #ifndef GQA_DECODE_SHORT_TILES
 #define GQA_DECODE_SHORT_TILES 24
 #endif
@@ -399,13 +407,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   ChunkDesc spec_first{};
   spec_first.u = -1;
   if (warp == kProducer) {
-    const bool guess = p.window == 0 && !p.evicting;
+    const bool guess = kGuessTiles > 0 && p.window == 0 && !p.evicting;
     if (lane == 0) {
       if (p.B > 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.seqlens) : "memory");
       if (guess) {
         const int items = p.B * p.Hkv;
-        const int item = c % items, t0 = (c / items) * kPrefetchTiles;
-        for (int t = t0; t < t0 + kPrefetchTiles && (t + 1) * kTile <= p.M; ++t) {
+        const int item = c % items, t0 = (c / items) * kGuessTiles;
+        for (int t = t0; t < t0 + kGuessTiles && (t + 1) * kTile <= p.M; ++t) {
           const size_t off = ((size_t)item * p.M + (size_t)t * kTile) * kD;
           bulk_prefetch_l2(static_cast<const T*>(p.kbuf) + off, kTile * kD * 2);
           bulk_prefetch_l2(static_cast<const T*>(p.vbuf) + off, kTile * kD * 2);
@@ -417,9 +425,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       spec_first = partition_and_locate_small(p, spec_len, c, lane, spec_pt);
       if (lane == 0 && spec_first.u >= 0) {
         const ChunkDesc& d = spec_first;
-        if (!guess) {
+        const int exact = guess ? kExactTiles : kPrefetchTiles;
+        if (exact > 0) {
           const int row0 = (d.b * p.Hkv + d.kh) * p.M + d.klo - (p.evicting ? slot0_position(d.L - 1, p.M) : 0);
-          for (int t = d.t0; t < min(d.t1, d.t0 + kPrefetchTiles); ++t) {
+          for (int t = d.t0; t < min(d.t1, d.t0 + exact); ++t) {
             const size_t off = ((size_t)row0 + (size_t)t * kTile) * kD;
             bulk_prefetch_l2(static_cast<const T*>(p.kbuf) + off, kTile * kD * 2);
             bulk_prefetch_l2(static_cast<const T*>(p.vbuf) + off, kTile * kD * 2);
