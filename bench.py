@@ -401,9 +401,9 @@ def cpu_baseline(name, min_seconds=10.0):
 # kernel per launch, from the ncu captures summarised in profiles/; a kernel
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
-    "decode_b16": 111428096 + 3087872,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
-    "prefill_2k": 112835328 + 33319936,    # prefill_kernel, profiles/prefill_kernel_prefill_2k.md
-    "chunked_prefill": 67845888 + 4827392,  # prefill_kernel, profiles/prefill_kernel_chunked_prefill.md
+    "decode_b16": 110934272 + 3039488,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
+    "prefill_2k": 112748800 + 33065216,    # prefill_head_kernel, profiles/prefill_head_kernel_prefill_2k.md
+    "chunked_prefill": 65930240 + 6252032,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
 }
 
 
@@ -472,11 +472,11 @@ def run_ours(args):
                     "bytes_per_launch": prob.bytes, "traffic": TRAFFIC.get(name),
                     "traffic_kernel": "decode_dyn_kernel"}
     else:
-        roofline = {"kernel": "rope_append_kernel + prefill_kernel (one gqa_forward call)", "bound": "tensor",
+        roofline = {"kernel": "rope_append_kernel + prefill_head_kernel (one gqa_forward call)", "bound": "tensor",
                     "achieved": rate, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": rate / pk["bf16_tflops"], "peak_source": pk["source"],
                     "flops_per_launch": prob.flops, "traffic": TRAFFIC.get(name),
-                    "traffic_kernel": "prefill_kernel"}
+                    "traffic_kernel": "prefill_head_kernel"}
 
     also = []
     if not args.no_also and not args.quick:
