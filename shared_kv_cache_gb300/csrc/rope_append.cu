@@ -81,8 +81,11 @@ __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
   using V = VecT<T, VEC>;
   // the attention kernel after this one (programmatic dependent launch)
   // may start its own prologue; it waits for this grid before it reads the
-  // buffer
+  // buffer.  This grid is itself launched that way: its CTAs may be resident
+  // before the kernel ahead of it (any kernel) has completed, and read
+  // nothing until it has.
   pdl_launch_dependents();
+  pdl_wait_primary();
   if (p.sched.base && blockIdx.x == 0) {
     psched::build(p.sched, p.sched_cap);
     return;
@@ -153,12 +156,18 @@ cudaError_t launch_t(const ForwardArgs& a, void* q_rot, void* k_new, const Prefi
                            ps->ipc, a.window, a.M, a.total, a.evict, ps->n_split, ps->target, ps->ktile};
     p.sched_cap = ps->cap;
   }
-  const dim3 grid(a.B * a.S + (ps ? 1 : 0));
-  if ((a.D / 2) % 8 == 0)
-    rope_append_kernel<T, 8><<<grid, 128, 0, a.stream>>>(p);
-  else
-    rope_append_kernel<T, 4><<<grid, 128, 0, a.stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * a.S + (ps ? 1 : 0)));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (a.D / 2) % 8 == 0 ? cudaLaunchKernelEx(&cfg, rope_append_kernel<T, 8>, p)
+                            : cudaLaunchKernelEx(&cfg, rope_append_kernel<T, 4>, p);
 }
 
 }  // namespace

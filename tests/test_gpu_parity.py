@@ -164,6 +164,60 @@ def test_prefill_cases(kw):
 
 
 # ---------------------------------------------------------------------------
+# Tensor-core prefill grids of at least two CTAs per CTA slot (B x H x
+# 128-token query tiles >= 2 x 2 x SMs): one CTA per work item, no work list
+# and no split key ranges (the cases above take the list)
+# ---------------------------------------------------------------------------
+def _full_grid(inp):
+    w = inp["workload"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    items = w.batch * w.num_heads * -(-w.seq_len // 128)
+    if items < 4 * sms:
+        pytest.skip(f"{items} work items do not fill two CTAs per slot on {sms} SMs")
+    # no work list, no partials: no scratch
+    dims = gqa.make_dims(w.batch, w.seq_len, w.num_heads, w.kv_num_heads, w.head_size, w.max_seq_len, w.dtype, 0,
+                         0 if inp["cos"] is None else inp["cos"].shape[0])
+    assert gqa.gqa_workspace_size(dims, inp["total_sequence_length"], inp["local_window_size"]) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    # ragged pasts around 64-key tiles; G = 10
+    dict(S=160, B=4, H=80, Hkv=8, past=(0, 37, 300, 1000), M=1200, dtype="fp16", seed=90),
+    # window, bias, interleaved rotary, bf16; G = 13
+    dict(S=300, B=2, H=104, Hkv=8, past=(5, 700), M=1100, window=100, bias=(1, 1), interleaved=1, dtype="bf16",
+         seed=91),
+    # no rotary; pasts at and next to tile edges
+    dict(S=129, B=5, H=64, Hkv=4, past=(0, 1, 63, 64, 65), M=256, rotary=False, dtype="fp16", seed=92),
+])
+def test_full_grid_prefill_cases(kw):
+    inp = custom(**kw)
+    _full_grid(inp)
+    check(inp)
+
+
+def test_full_grid_prefill_device_overflow_skips_that_sequence():
+    """One sequence's past + new exceeds max_seq_len (the host is told a
+    total that fits): the error word says so, that sequence's buffer rows and
+    output rows are untouched, and the others match the oracle."""
+    kw = dict(S=128, B=4, H=152, Hkv=8, M=4096, total=4096, dtype="fp16", seed=93)
+    inp = custom(past=(0, 3969, 100, 3968), **kw)
+    _full_grid(inp)
+    kb0, vb0 = W.bits(inp["k_buf"]).copy(), W.bits(inp["v_buf"]).copy()
+    st, dst, out, kb, vb = run_cuda(inp)
+    assert st == gqa.GQA_OK and dst == gqa.GQA_ERR_KV_OVERFLOW
+    assert np.array_equal(W.bits(kb)[1], kb0[1]) and np.array_equal(W.bits(vb)[1], vb0[1])
+    assert torch.isnan(out[1].float()).all()
+    keep = [0, 2, 3]
+    ok = custom(past=(0, 100, 3968), **{**kw, "B": 3})
+    for n in ("query", "key", "value", "k_buf", "v_buf"):
+        ok[n] = inp[n][keep].contiguous()
+    ref = run_oracle(ok)
+    assert np.array_equal(W.bits(kb)[keep], ref[2]) and np.array_equal(W.bits(vb)[keep], ref[3])
+    got = out[keep].double().numpy()
+    assert np.abs(got - ref[1].reshape(got.shape)).max() <= 2e-3
+
+
+# ---------------------------------------------------------------------------
 # Non-shared binding: separate past [B, Hkv, Mp, D] and present buffers; the
 # present becomes past + new
 # ---------------------------------------------------------------------------
