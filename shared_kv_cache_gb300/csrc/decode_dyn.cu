@@ -232,8 +232,10 @@ __device__ __forceinline__ int chunk_target(const DynParams& p, int T) {
 // tiles, then (when C does not divide its tiles) one shorter remainder chunk.
 // Chunks are numbered all whole chunks first, then all remainders, so the
 // chunks handed out last by the ticket are the short ones and the CTAs'
-// end times stay close.  An item of n >= 2 chunks keeps n partial slots,
-// whole chunks first.
+// end times stay close.  In a batch of at most 32 sequences the remainders
+// go longest first (ties: lower sequence first), so that the very last ones
+// are the shortest.  An item of n >= 2 chunks keeps n partial slots, whole
+// chunks first.
 struct Partition {
   int C;
   int UA, U;  // whole chunks; all chunks
@@ -265,18 +267,40 @@ __device__ Partition make_partition(const DynParams& p, const int* sl, int lane)
   return pt;
 }
 
+// The first remainder chunk of lane's sequence when a batch of at most 32
+// sequences takes its remainders longest first: the remainders (`ch` chunks
+// of `rlen` tiles per lane) of every lane that sorts before this one.
+__device__ __forceinline__ int rem_sorted_start(int rlen, int ch, int lane) {
+  int start = 0;
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    const int ri = __shfl_sync(0xffffffffu, rlen, i);
+    const int ci = __shfl_sync(0xffffffffu, ch, i);
+    if (ri > rlen || (ri == rlen && i < lane)) start += ci;
+  }
+  return start;
+}
+
 // Chunk u within one block of 32 sequences b0 + lane.  Each lane brings its
 // sequence's tile count, key range and chunk counts; incl / sincl are the
 // block's inclusive scans of this group's chunks and of partial slots, cbase
-// / sbase those of earlier blocks; v counts chunks within the group.
+// / sbase those of earlier blocks; v counts chunks within the group.  With
+// `sorted` (remainders of a batch of at most 32 sequences) the group is in
+// the longest-first order instead of the sequence order.
 __device__ __forceinline__ ChunkDesc chunk_in_block(const DynParams& p, const Partition& pt, int u, int v, bool rem,
                                                     int b0, int tb, int lo, int L, int nA, int nB, int ch, int sl_n,
-                                                    int incl, int sincl, int cbase, int sbase) {
-  const unsigned m = __ballot_sync(0xffffffffu, cbase + incl > v);
-  const int l = __ffs(m) - 1;
+                                                    int incl, int sincl, int cbase, int sbase, bool sorted) {
+  int l, c0;
+  if (rem && sorted) {
+    const int st = rem_sorted_start(nB ? tb - nA * pt.C : 0, ch, threadIdx.x & 31);
+    l = __ffs(__ballot_sync(0xffffffffu, ch > 0 && st <= v && v < st + ch)) - 1;
+    c0 = __shfl_sync(0xffffffffu, st, l);
+  } else {
+    l = __ffs(__ballot_sync(0xffffffffu, cbase + incl > v)) - 1;
+    c0 = cbase + __shfl_sync(0xffffffffu, incl - ch, l);
+  }
   ChunkDesc d;
   d.b = b0 + l;
-  const int c0 = cbase + __shfl_sync(0xffffffffu, incl - ch, l);
   const int s0 = sbase + __shfl_sync(0xffffffffu, sincl - sl_n, l);
   d.tb = __shfl_sync(0xffffffffu, tb, l);
   d.klo = __shfl_sync(0xffffffffu, lo, l);
@@ -318,7 +342,7 @@ __device__ ChunkDesc partition_and_locate_small(const DynParams& p, int len, int
   const int sl_n = nA + nB > 1 ? (nA + nB) * p.Hkv : 0;
   const int incl = warp_incl_scan(ch, lane);
   const int sincl = warp_incl_scan(sl_n, lane);
-  return chunk_in_block(p, pt, u, v, rem, 0, tb, lo, L, nA, nB, ch, sl_n, incl, sincl, 0, 0);
+  return chunk_in_block(p, pt, u, v, rem, 0, tb, lo, L, nA, nB, ch, sl_n, incl, sincl, 0, 0, true);
 }
 
 // Warp-cooperative: the item and tile range of chunk u (< U).
@@ -337,7 +361,7 @@ __device__ ChunkDesc locate_chunk(const DynParams& p, const int* sl, const Parti
     const int sincl = warp_incl_scan(sl_n, lane);
     const int chunk_total = __shfl_sync(0xffffffffu, incl, 31);
     if (v < cbase + chunk_total)
-      return chunk_in_block(p, pt, u, v, rem, b0, tb, lo, L, nA, nB, ch, sl_n, incl, sincl, cbase, sbase);
+      return chunk_in_block(p, pt, u, v, rem, b0, tb, lo, L, nA, nB, ch, sl_n, incl, sincl, cbase, sbase, p.B <= 32);
     cbase += chunk_total;
     sbase += __shfl_sync(0xffffffffu, sincl, 31);
   }
@@ -613,8 +637,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       cnt = __shfl_sync(0xffffffffu, cnt, 0);
       if (cnt != (uint32_t)(n - 1)) continue;
-      // the item's last chunk: merge its n partials (read through L2)
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      // the item's last chunk: merge its n partials (read through L2; the
+      // warp barrier orders lane 0's acquiring count before every lane's loads)
+      __syncwarp();
       T* outg = static_cast<T*>(p.out) + ((size_t)b * p.H + (size_t)kh * G) * kD;
       const float* ml0 = p.part_ml + (size_t)first * G * 2;
       const float* po0 = p.part_o + (size_t)first * G * kD;
