@@ -20,8 +20,11 @@
 //
 // Inside a CTA (256 threads):
 //   warp 0      bulk-tensor (TMA) loads: the query tile once, the tile's
-//               cos/sin rows, then K and V tiles of 64 keys through two
-//               2-stage rings;
+//               cos/sin rows, then K tiles of 64 keys through a 2-stage
+//               ring;
+//   warp 2      the V tiles, through their own 2-stage ring (one thread
+//               per ring, so that a K copy goes out as soon as its stage
+//               is free, not after the V copy before it);
 //   warp 1      owns TMEM; lane 0 issues S = Q K^T into one of two S buffers
 //               and O += P V with P in TMEM and V MN-major, in the order
 //                 S(0), S(1), P(0) V_0, S(2), P(1) V_1, S(3), ...
@@ -32,7 +35,7 @@
 //               registers), mask, take the max, exponentiate, sum, write P
 //               (16-bit) over S; O is rescaled in TMEM only when the row max
 //               grew by more than 2^8.
-//   (warps 2 and 3 have no role; the register split favours the softmax.)
+//   (warp 3 has no role; the register split favours the softmax.)
 // TMEM columns: O [0, 128), S0 [128, 192), S1 [192, 256).  At the end the
 // query buffer holds the output rows for the bulk-tensor stores.
 #include <type_traits>
@@ -48,7 +51,12 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBM = 128;                    // query rows per tile
 constexpr int kBN = 64;                     // keys per KV tile
-constexpr int kKSt = 2;                     // K ring stages
+// (three K stages fit beside two CTAs per SM too, but ran slower: more
+// copies in flight only lengthened each copy)
+#ifndef GQA_PREFILL_K_STAGES
+#define GQA_PREFILL_K_STAGES 2
+#endif
+constexpr int kKSt = GQA_PREFILL_K_STAGES;  // K ring stages
 constexpr int kVSt = 2;                     // V ring stages
 constexpr int kThreads = 256;               // eight warps
 constexpr int kRegsLow = 56;                // warps 0..3 after setmaxnreg
@@ -66,9 +74,17 @@ constexpr int kSinOff = kVOff + kTileBytes;  // V stage 1, likewise
 // q_ready, cs_full, m_full (one s_full and one p_full per S buffer: a barrier
 // then never runs two phases ahead of its waiter)
 constexpr int kNumBars = 1 + 2 * kKSt + 2 * kVSt + 2 + 2 + 1 + 1 + 1 + 1 + 1;
-constexpr int kBarOff = kVOff + kVSt * kTileBytes;
-constexpr int kSlotOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kSlotOff + 16 + 1024;
+constexpr int kTilesBytes = kVOff + kVSt * kTileBytes;  // from the 1024-byte aligned start
+// the barriers and the TMEM address slot ("meta"): in the alignment padding
+// before the tiles when it is large enough, else after the tiles
+constexpr int kSlotOff = kNumBars * 8;  // within the meta block
+constexpr int kMetaBytes = 256;
+static_assert(kSlotOff + 16 <= kMetaBytes, "meta block");
+// the tiles start at the first 1024-byte boundary of the dynamic shared
+// memory (at most 1008 bytes in, from a 16-byte aligned start); the meta
+// block goes into that padding if it fits there, else after the tiles
+constexpr int kSmemBytes = kTilesBytes + 1024;
+static_assert(kSmemBytes >= kTilesBytes + 768 + kMetaBytes, "meta after the tiles when the padding is short");
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 static_assert(psched::kQTile == kBM && kPrefillKeyTile == kBN, "tile sizes");
 constexpr uint32_t kTmemCols = 256;
@@ -191,10 +207,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const HeadParams p) {
   using E = Elem<T>;
   constexpr bool kBF16 = E::is_bf16;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* meta = (smem - smem_raw) >= kMetaBytes ? smem_raw : smem + kTilesBytes;
   const uint32_t sb = smem_u32(smem);
-  const uint32_t bar0 = sb + kBarOff;
+  const uint32_t bar0 = smem_u32(meta);
   const uint32_t q_full = bar0;
   const uint32_t k_full = bar0 + 8, k_empty = k_full + 8 * kKSt;
   const uint32_t v_full = k_empty + 8 * kKSt, v_empty = v_full + 8 * kVSt;
@@ -206,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t cs_full = q_ready + 8;      // the cos / sin rows
   const uint32_t m_full = cs_full + 8;       // another piece's partial, for the merge
   const bool rot = p.cos != nullptr;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kSlotOff);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(meta + kSlotOff);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -301,37 +318,35 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-    if (warp == 0) {
-      // ---------------- producer ----------------
+    if (warp == 0 || warp == 2) {
+      // ---------------- producers: K tiles (warp 0), V tiles (warp 2) ----------------
       if (lane == 0) {
-        prefetch_tensormap(&kmap);
-        prefetch_tensormap(&vmap);
+        const bool is_k = warp == 0;
+        const CUtensorMap* map = is_k ? &kmap : &vmap;
+        const uint32_t full = is_k ? k_full : v_full, empty = is_k ? k_empty : v_empty;
+        const uint32_t ring = sb + (is_k ? kKOff : kVOff);
+        const int nst = is_k ? kKSt : kVSt;  // ring stages
+        prefetch_tensormap(map);
         pdl_wait_primary();  // the new K/V rows are the append kernel's
         const int zkv = b * p.Hkv + kh;
-        int issued_k = 0, issued_v = 0;
+        int issued = 0;
         for (int j = 0; j < n_kv; ++j) {
           const int y = kbase + j * kBN;
-          const int ks = j % kKSt, vs = j % kVSt;
+          const int st = j % nst;
           // K / V stage 1 hold the cos / sin rows until the query rows are rotated
           if (j == 1 && rot && !mbar_wait(q_ready, 0, p.err)) break;
-          if (j >= kKSt && !mbar_wait(k_empty + 8 * ks, ((j / kKSt) - 1) & 1, p.err)) break;
-          mbar_arrive_expect_tx(k_full + 8 * ks, kTileBytes);
-          tma_load_3d(sb + kKOff + ks * kTileBytes, &kmap, 0, y, zkv, k_full + 8 * ks);
-          tma_load_3d(sb + kKOff + ks * kTileBytes + kKVBox, &kmap, 64, y, zkv, k_full + 8 * ks);
-          issued_k = j + 1;
-          if (j >= kVSt && !mbar_wait(v_empty + 8 * vs, ((j / kVSt) - 1) & 1, p.err)) break;
-          mbar_arrive_expect_tx(v_full + 8 * vs, kTileBytes);
-          tma_load_3d(sb + kVOff + vs * kTileBytes, &vmap, 0, y, zkv, v_full + 8 * vs);
-          tma_load_3d(sb + kVOff + vs * kTileBytes + kKVBox, &vmap, 64, y, zkv, v_full + 8 * vs);
-          issued_v = j + 1;
+          if (j >= nst && !mbar_wait(empty + 8 * st, ((j / nst) - 1) & 1, p.err)) break;
+          mbar_arrive_expect_tx(full + 8 * st, kTileBytes);
+          tma_load_3d(ring + st * kTileBytes, map, 0, y, zkv, full + 8 * st);
+          tma_load_3d(ring + st * kTileBytes + kKVBox, map, 64, y, zkv, full + 8 * st);
+          issued = j + 1;
         }
         // no copy may still be in flight into shared memory when the CTA exits
-        mbar_wait(q_full, 0, p.err);
-        if (rot) mbar_wait(cs_full, 0, p.err);
-        for (int j = max(0, issued_k - kKSt); j < issued_k; ++j)
-          mbar_wait(k_full + 8 * (j % kKSt), (j / kKSt) & 1, p.err);
-        for (int j = max(0, issued_v - kVSt); j < issued_v; ++j)
-          mbar_wait(v_full + 8 * (j % kVSt), (j / kVSt) & 1, p.err);
+        if (is_k) {
+          mbar_wait(q_full, 0, p.err);
+          if (rot) mbar_wait(cs_full, 0, p.err);
+        }
+        for (int j = max(0, issued - nst); j < issued; ++j) mbar_wait(full + 8 * (j % nst), (j / nst) & 1, p.err);
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -400,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_wait(drain, 0, p.err);
       }
       __syncwarp();
-    }  // warps 2 and 3 have no role
+    }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     // ---------------- softmax warps 4..7 ----------------
