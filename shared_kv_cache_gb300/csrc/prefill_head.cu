@@ -51,13 +51,16 @@ namespace {
 constexpr int kD = 128;
 constexpr int kBM = 128;                    // query rows per tile
 constexpr int kBN = 64;                     // keys per KV tile
-// (three K stages fit beside two CTAs per SM too, but ran slower: more
-// copies in flight only lengthened each copy)
+// (a third K or V stage fits beside two CTAs per SM too, but either ran
+// slower: more copies in flight only lengthened each copy)
 #ifndef GQA_PREFILL_K_STAGES
 #define GQA_PREFILL_K_STAGES 2
 #endif
 constexpr int kKSt = GQA_PREFILL_K_STAGES;  // K ring stages
-constexpr int kVSt = 2;                     // V ring stages
+#ifndef GQA_PREFILL_V_STAGES
+#define GQA_PREFILL_V_STAGES 2
+#endif
+constexpr int kVSt = GQA_PREFILL_V_STAGES;  // V ring stages
 constexpr int kThreads = 256;               // eight warps
 constexpr int kRegsLow = 56;                // warps 0..3 after setmaxnreg
 constexpr int kRegsHigh = 200;              // warps 4..7: 128 * 56 + 128 * 200 = 256 * 128
