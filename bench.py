@@ -401,9 +401,9 @@ def cpu_baseline(name, min_seconds=10.0):
 # kernel per launch, from the ncu captures summarised in profiles/; a kernel
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
-    "decode_b16": 110934272 + 3039488,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
-    "prefill_2k": 112748800 + 33065216,    # prefill_head_kernel, profiles/prefill_head_kernel_prefill_2k.md
-    "chunked_prefill": 65930240 + 6252032,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
+    "decode_b16": 111111680 + 3026944,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
+    "prefill_2k": 113376768 + 33452800,    # prefill_head_kernel, profiles/prefill_head_kernel_prefill_2k.md
+    "chunked_prefill": 65953280 + 6172416,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
 }
 
 
