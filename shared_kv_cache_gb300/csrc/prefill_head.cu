@@ -301,6 +301,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_kv = kSched ? n_l : n_all;
   const bool split = kSched && k_pieces > 1;  // partial results, merged by the item's last piece
   const int kbase = kstart + t_lo * kBN;
+  // Without the list the query heads of a KV head walk its key tiles from
+  // different starting tiles (head h % G starts at tile (h % G) n / G and
+  // wraps), so that they do not all ask L2 for the same tile at once (the
+  // online softmax takes the tiles in any order).  The list's pieces keep
+  // the plain order: their tiles come from DRAM, where the heads' requests
+  // for the same tile share one read.
+  const int trot = (!kSched && n_kv > 0) ? ((h % p.G) * n_kv / p.G) % n_kv : 0;
+  auto tpos = [&](int jj) {
+    const int t = jj + trot;
+    return kbase + (t >= n_kv ? t - n_kv : t) * kBN;
+  };
   // bf16 tiles whose first row sees few keys also carry P's rounding residue
   // (P = hi + lo, both bf16; lo in the upper half of the S buffer) so that
   // P.V keeps fp32-level accuracy where a few keys dominate the output
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int zkv = b * p.Hkv + kh;
         int issued = 0;
         for (int j = 0; j < n_kv; ++j) {
-          const int y = kbase + j * kBN;
+          const int y = tpos(j);
           const int st = j % nst;
           // K / V stage 1 hold the cos / sin rows until the query rows are rotated
           if (j == 1 && rot && !mbar_wait(q_ready, 0, p.err)) break;
@@ -437,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // 8 keys: a multiple of 8 like kbase, below kend rounded up to 8 <= total)
     uint4 bnext[8];
     auto fetch_bias = [&](int j) {
-      const int k0 = kbase + j * kBN;
+      const int k0 = tpos(j);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         bnext[q] = k0 + 8 * q < kend ? __ldg(reinterpret_cast<const uint4*>(brow + k0 + 8 * q)) : make_uint4(0, 0, 0, 0);
@@ -460,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const float bias_unit = kLog2e / p.scale_log2;  // bias in raw score units (scale > 0)
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int k0 = kbase + j * kBN;
+      const int k0 = tpos(j);
       const uint32_t tS = tbase + kColS + (j & 1) * 64 + lane_off;
       if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * (j & 1), (j >> 1) & 1, p.err))) { ok = false; break; }
       tc::fence_after();
