@@ -402,9 +402,11 @@ def cpu_baseline(name, min_seconds=10.0):
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
     "decode_b16": 111111680 + 3026944,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
-    "prefill_2k": 113376768 + 33452800,    # prefill_head_kernel, profiles/prefill_head_kernel_prefill_2k.md
     "chunked_prefill": 65953280 + 6172416,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
 }
+# the attention kernel of each prefill workload: two query heads per CTA
+# where the group size is even and there is no bias or window
+PREFILL_KERNEL = {"prefill_2k": "prefill_dual_kernel", "chunked_prefill": "prefill_head_kernel"}
 
 
 def metric_of(prob):
@@ -472,11 +474,12 @@ def run_ours(args):
                     "bytes_per_launch": prob.bytes, "traffic": TRAFFIC.get(name),
                     "traffic_kernel": "decode_dyn_kernel"}
     else:
-        roofline = {"kernel": "rope_append_kernel + prefill_head_kernel (one gqa_forward call)", "bound": "tensor",
+        kern = PREFILL_KERNEL.get(name, "prefill_head_kernel")
+        roofline = {"kernel": f"rope_append_kernel + {kern} (one gqa_forward call)", "bound": "tensor",
                     "achieved": rate, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": rate / pk["bf16_tflops"], "peak_source": pk["source"],
                     "flops_per_launch": prob.flops, "traffic": TRAFFIC.get(name),
-                    "traffic_kernel": "prefill_head_kernel"}
+                    "traffic_kernel": kern}
 
     also = []
     if not args.no_also and not args.quick:

@@ -16,7 +16,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgqa.so")
 
 SOURCES = ["gqa_api.cu", "rope_append.cu", "attn_generic.cu", "decode_splitkv.cu", "decode_dyn.cu", "decode_noalloc.cu", "host_io.cu", "present_copy.cu", "evict_shift.cu",
-           "prefill_head.cu"]
+           "prefill_head.cu", "prefill_dual.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

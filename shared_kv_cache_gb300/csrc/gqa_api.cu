@@ -55,6 +55,11 @@ int sm_count() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+#ifndef GQA_PREFILL_DUAL
+#define GQA_PREFILL_DUAL 1
+#endif
+constexpr bool kPrefillDual = GQA_PREFILL_DUAL != 0;  // the two-head prefill kernel where it applies
+
 // A fresh tag for the decode counters in the workspace, per call (never 0,
 // the value the kernel leaves behind, nor all ones).
 uint32_t next_epoch() {
@@ -394,8 +399,11 @@ gqa_status_t forward_impl(const gqa_dims_t* dims, const void* query, const void*
                             kPrefillKeyTile};
       const PrefillSched* psp = pl.path == Path::kPrefillTC && pl.sched_cap > 0 ? &ps : nullptr;
       e = launch_rope_append(a, q_rot, k_new, psp);
+      // without the work list, the two-head kernel where it applies
+      const bool dual = kPrefillDual && pl.path == Path::kPrefillTC && !psp && prefill_dual_applies(a);
       if (e == cudaSuccess)
-        e = pl.path == Path::kPrefillTC
+        e = dual ? launch_prefill_dual(a, query)
+            : pl.path == Path::kPrefillTC
                 ? launch_prefill_head(a, query, pl.splits, reinterpret_cast<float*>(ws + pl.part_o_off),
                                       reinterpret_cast<float*>(ws + pl.part_ml_off), psp)
                 : launch_attn_generic(a, q_rot ? q_rot : query, k_new);

@@ -118,6 +118,11 @@ constexpr int kPrefillKeyTile = 64;  // keys per K/V tile of the prefill kernel
 cudaError_t launch_prefill_head(const ForwardArgs& a, const void* q_src, int n_split, float* part_o, float* part_ml,
                                 const PrefillSched* sched = nullptr);
 int prefill_head_splits(int B, int S, int H, int total, int num_sms);
+// Tensor-core prefill with two query heads of a KV head per CTA, one CTA per
+// SM and 128-key tiles (prefill_dual.cu): for head size 128, an even group
+// size, no window and no attention_bias, on grids without the work list.
+bool prefill_dual_applies(const ForwardArgs& a);
+cudaError_t launch_prefill_dual(const ForwardArgs& a, const void* q_src);
 size_t prefill_head_split_rows(int B, int S, int H, int n_split);
 
 // Staging copies of up to kMaxStageSegs byte ranges (each a multiple of 4

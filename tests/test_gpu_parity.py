@@ -188,6 +188,11 @@ def _full_grid(inp):
          seed=91),
     # no rotary; pasts at and next to tile edges
     dict(S=129, B=5, H=64, Hkv=4, past=(0, 1, 63, 64, 65), M=256, rotary=False, dtype="fp16", seed=92),
+    # the two-head kernel (even group size, no window, no bias): bf16 rows
+    # that see few keys (P's residue), interleaved rotary; G = 20
+    dict(S=256, B=2, H=160, Hkv=8, past=(0, 100), M=512, interleaved=1, dtype="bf16", seed=94),
+    # ragged query tiles (S = 300) and 128-key tiles straddling the past; G = 26
+    dict(S=300, B=2, H=104, Hkv=4, past=(5, 700), M=1100, dtype="fp16", seed=95),
 ])
 def test_full_grid_prefill_cases(kw):
     inp = custom(**kw)
@@ -195,11 +200,12 @@ def test_full_grid_prefill_cases(kw):
     check(inp)
 
 
-def test_full_grid_prefill_device_overflow_skips_that_sequence():
+@pytest.mark.parametrize("H", [152, 160])  # group sizes 19 (one head per CTA) and 20 (two)
+def test_full_grid_prefill_device_overflow_skips_that_sequence(H):
     """One sequence's past + new exceeds max_seq_len (the host is told a
     total that fits): the error word says so, that sequence's buffer rows and
     output rows are untouched, and the others match the oracle."""
-    kw = dict(S=128, B=4, H=152, Hkv=8, M=4096, total=4096, dtype="fp16", seed=93)
+    kw = dict(S=128, B=4, H=H, Hkv=8, M=4096, total=4096, dtype="fp16", seed=93)
     inp = custom(past=(0, 3969, 100, 3968), **kw)
     _full_grid(inp)
     kb0, vb0 = W.bits(inp["k_buf"]).copy(), W.bits(inp["v_buf"]).copy()
