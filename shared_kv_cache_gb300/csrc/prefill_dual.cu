@@ -80,8 +80,9 @@ constexpr int kCosOff = kVOff + kSt * kTileBytes;  // the item's 128 cos rows (6
 constexpr int kSinOff = kCosOff + kBM * 128;        // and sin rows
 constexpr int kTilesBytes = kSinOff + kBM * 128;    // 224 KB, from the 1024-byte aligned start
 // barriers: q_full, cs_full, q_ready, drain, q_free, k_full[2], k_empty[2], v_full[2], v_empty[2],
-// s_full[2], p_full[2], o_done[2], o_free[2] (one s_full / p_full / o_done / o_free per head)
-constexpr int kNumBars = 5 + 4 * kSt + 8;
+// s_full[2], p_full[2], o_done[2], o_free[2] (one s_full / p_full / o_done / o_free per head),
+// stage_free
+constexpr int kNumBars = 5 + 4 * kSt + 8 + 1;
 constexpr int kSlotOff = kNumBars * 8;      // the TMEM address, within the meta block
 constexpr int kMetaBytes = 256;
 static_assert(kSlotOff + 16 <= kMetaBytes, "meta block");
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t p_full = s_full + 16;        // [2]
   const uint32_t o_done = p_full + 16;        // [2]
   const uint32_t o_free = o_done + 16;        // [2]
+  const uint32_t stage_free = o_free + 16;    // the output stage read by its copies (per item)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(meta + kSlotOff);
   const bool rot = p.cos != nullptr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_done + 8 * i, 1);
       mbar_init(o_free + 8 * i, 128);
     }
+    mbar_init(stage_free, 8);
     fence_mbar_init();
   }
   if (warp == 1) tc::alloc(smem_u32(tslot), kTmemCols);
@@ -223,23 +226,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Item w = decode_item(p, it);
           if (w.skip) continue;
           if (is_q) {
-            // the query buffers are free once the previous item's score MMAs
-            // are done, the cos/sin rows once its rows are rotated
-            if (kq > 0 && !(mbar_wait(q_free, (kq - 1) & 1, p.err) && mbar_wait(q_ready, (kq - 1) & 1, p.err))) {
+            // Neither barrier may run a phase ahead of the softmax warps'
+            // waits: both wait for the previous item's rows to be rotated.
+            if (kq > 0 && !mbar_wait(q_ready, (kq - 1) & 1, p.err)) {
               ok = false;
               break;
-            }
-            mbar_arrive_expect_tx(q_full, 2 * kQBytes);
-            for (int i = 0; i < 2; ++i) {
-              pf::tma_load_4d(sb + kQOff + i * kQBytes, &qmap, 0, w.h0 + i, w.i0, w.b, q_full);
-              pf::tma_load_4d(sb + kQOff + i * kQBytes + kQBox, &qmap, 64, w.h0 + i, w.i0, w.b, q_full);
             }
             if (rot) {
               // the cos / sin rows of positions past + i0 .. + 127 (rows past
               // the cache's end read as zeros and are never used), once the
-              // output of the item two back has left the area
-              if (kq >= 2 &&
-                  !(mbar_wait(o_free, (kq - 2) & 1, p.err) && mbar_wait(o_free + 8, (kq - 2) & 1, p.err))) {
+              // output of the item two back has left the area: about an item
+              // ahead of their use
+              if (kq >= 2 && !mbar_wait(stage_free, (kq - 2) & 1, p.err)) {
                 ok = false;
                 break;
               }
@@ -249,6 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               mbar_arrive(cs_full);
             }
+            // the query buffers are free once the previous item's score MMAs
+            // are done; both heads' tiles in one box
+            if (kq > 0 && !mbar_wait(q_free, (kq - 1) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(q_full, 2 * kQBytes);
+            pf::tma_load_5d(sb + kQOff, &qmap, 0, w.i0, 0, w.h0, w.b, q_full);
             ++kq;
           }
           if (is_q) continue;
@@ -536,6 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_before();
         mbar_arrive(pf_bar);
+        if (j == 0 && kq > 0) {
+          // the previous item's output copies have long read the stage
+          if (lane == 0) {
+            pf::bulk_wait_read_all();
+            mbar_arrive(stage_free);
+          }
+          __syncwarp();
+        }
       }
       if (!ok) break;
       // the next item's query rows are rotated before this item's output is
@@ -545,11 +559,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool have2 = next_item(k, w2);
       if (have2 && !rotate(w2, kq + 1)) { ok = false; break; }
       // the item's output, once its MMAs have completed: O / l of this row
-      // as 16-bit values, staged per warp (32 rows x 64 dims, 128-byte
-      // swizzled) in the cos / sin area and written by bulk-tensor stores
-      // (rows past S are clipped by the copy).  The area is free: the next
-      // item's rows are rotated by both heads (its rows stay until the
-      // producer sees this item's o_free arrivals).
+      // as 16-bit values, in four passes of 32 dimensions, each staged per
+      // warp (32 rows x 64 bytes, 64-byte swizzled; two stages a warp) in
+      // the cos / sin area and written by a bulk-tensor store (rows past S
+      // are clipped by the copy).  The area is free: the next item's rows
+      // are rotated by both heads, and the producer refills it only after
+      // this item's stage_free arrivals.
       bool done = mbar_wait(drain, kq & 1, p.err);
       if (have2 && rot) done = done && mbar_wait(q_ready, (kq + 1) & 1, p.err);
       if (!__all_sync(0xffffffffu, done)) { ok = false; break; }
@@ -557,36 +572,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv = 1.f / l_run;
       const int r0 = w.i0 + 32 * (warp & 3);  // the warp's first row
       const uint32_t stg = sb + kCosOff + (warp - 4) * 4096;
-      uint8_t* srow = smem + kCosOff + (warp - 4) * 4096 + lane * 128;
+      uint8_t* srow = smem + kCosOff + (warp - 4) * 4096 + lane * 64;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t r[2][32];
-        tc::ld32(tO + 64 * hf, r[0]);
-        tc::ld32(tO + 64 * hf + 32, r[1]);
+      for (int qp = 0; qp < 4; ++qp) {
+        uint32_t r[32];
+        tc::ld32(tO + 32 * qp, r);
         tc::wait_ld();
-        if (hf == 1) {
-          if (lane == 0) pf::bulk_wait_read_all();  // the first half's copy has read the stage
-          __syncwarp();
-        }
+        if (lane == 0) pf::bulk_wait_read_1();  // the copy two passes back has read this stage
+        __syncwarp();
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // dims 64 hf + 8 c .. + 7
-          const uint32_t* rr = r[c >> 2] + 8 * (c & 3);
+        for (int c = 0; c < 4; ++c) {  // dims 32 qp + 8 c .. + 7
+          const uint32_t* rr = r + 8 * c;
           uint4 v;
           v.x = E::pack2(__uint_as_float(rr[0]) * inv, __uint_as_float(rr[1]) * inv);
           v.y = E::pack2(__uint_as_float(rr[2]) * inv, __uint_as_float(rr[3]) * inv);
           v.z = E::pack2(__uint_as_float(rr[4]) * inv, __uint_as_float(rr[5]) * inv);
           v.w = E::pack2(__uint_as_float(rr[6]) * inv, __uint_as_float(rr[7]) * inv);
-          *reinterpret_cast<uint4*>(srow + ((c ^ (lane & 7)) << 4)) = v;
+          *reinterpret_cast<uint4*>(srow + (qp & 1) * 2048 + ((c ^ ((lane >> 1) & 3)) << 4)) = v;
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && r0 < p.S) {
-          pf::tma_store_4d(&omap, stg, 64 * hf, w.h0 + hd, r0, w.b);
+          pf::tma_store_4d(&omap, stg + (qp & 1) * 2048, 32 * qp, w.h0 + hd, r0, w.b);
           pf::bulk_commit();
         }
       }
-      if (lane == 0) pf::bulk_wait_read_all();
-      __syncwarp();
+      // O is read: the next item's first P·V may overwrite it
       tc::fence_before();
       mbar_arrive(o_free + 8 * hd);
       ++kq;
@@ -613,16 +624,20 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
   {
     const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.S, (cuuint64_t)a.B};
     const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.H * kD * 2, (cuuint64_t)a.S * a.H * kD * 2};
-    const cuuint32_t box[4] = {64, 1, 32, 1};  // one warp's 32 rows
-    if (!encode_tensor_map(&omap, dt, 4, a.out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    const cuuint32_t box[4] = {32, 1, 32, 1};  // 32 dimensions of one warp's 32 rows
+    if (!encode_tensor_map(&omap, dt, 4, a.out, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
       return cudaErrorInvalidValue;
   }
   {
-    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)a.H, (cuuint64_t)a.S, (cuuint64_t)a.B};
-    // token rows a.q_stride elements apart (H * D, or (H + 2 Hkv) * D packed)
-    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)a.q_stride * 2, (cuuint64_t)a.S * a.q_stride * 2};
-    const cuuint32_t box[4] = {64, 1, (cuuint32_t)kBM, 1};
-    if (!encode_tensor_map(&qmap, dt, 4, const_cast<void*>(q_src), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    // (dimension within a half, token, half, head, sequence); token rows
+    // a.q_stride elements apart (H * D, or (H + 2 Hkv) * D packed): a box of
+    // 128 tokens, both halves and two heads lands as the two heads' tiles,
+    // each two [128 rows x 64 dims] boxes
+    const cuuint64_t dims[5] = {64, (cuuint64_t)a.S, 2, (cuuint64_t)a.H, (cuuint64_t)a.B};
+    const cuuint64_t strides[4] = {(cuuint64_t)a.q_stride * 2, 128, (cuuint64_t)kD * 2,
+                                   (cuuint64_t)a.S * a.q_stride * 2};
+    const cuuint32_t box[5] = {64, (cuuint32_t)kBM, 2, 2, 1};
+    if (!encode_tensor_map(&qmap, dt, 5, const_cast<void*>(q_src), dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   {
