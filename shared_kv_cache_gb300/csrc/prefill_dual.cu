@@ -28,11 +28,13 @@
 // rotation, which the softmax warps do before the current item's output
 // (so the next item's first score MMAs run while that output is written).
 // Inside a CTA (384 threads):
-//   warp 0       bulk-tensor (TMA) loads: each item's two query tiles (once
-//                the previous item's last score MMA has read its own) and
-//                cos/sin rows, then its K tiles of 128 keys through a
-//                2-stage ring that runs across items;
-//   warp 2       the V tiles, through their own 2-stage ring;
+//   warp 0       bulk-tensor (TMA) loads of the K tiles, 128 keys each (one
+//                4-D box for both 64-dimension halves), through a 2-stage
+//                ring that runs across items;
+//   warps 2, 3   the V tiles through their own 2-stage ring, one half each;
+//                warp 3 first loads each item's cos/sin rows (an item ahead)
+//                and its two query tiles (one 5-D box, once the previous
+//                item's last score MMA has read its own);
 //   warp 1       owns TMEM and issues, for tile j, P0(j) V_j, S0(j+1),
 //                P1(j) V_j, S1(j+1) (head 0's next scores while head 1's
 //                softmax runs, and the other way round);
@@ -41,9 +43,10 @@
 //                128 scores, mask, take the max, exponentiate, sum, write P
 //                (16-bit) over S; O is rescaled in TMEM only when the row
 //                max grew by more than 2^8; at the item's end, after the
-//                next item's rotation, O / l goes from TMEM through a per-warp
-//                stage in the (then unused) cos/sin area to the output rows
-//                by bulk-tensor stores;
+//                next item's rotation, O / l goes from TMEM to the output
+//                rows in four 32-dimension passes, each staged per warp in
+//                the (then unused) cos/sin area and written by a bulk-tensor
+//                store;
 //   warps 8..11  head 1's softmax, likewise.
 // TMEM columns: head i's O at [256 i, 256 i + 128), its S at
 // [256 i + 128, 256 i + 256).  Every barrier's phase counts items or tiles
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kSt; ++s) {
       mbar_init(k_full + 8 * s, 1);
       mbar_init(k_empty + 8 * s, 1);
-      mbar_init(v_full + 8 * s, 1);
+      mbar_init(v_full + 8 * s, 2);  // the two halves' producers
       mbar_init(v_empty + 8 * s, 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -199,10 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp != 1) {
-      // ---------------- producers: K tiles (warp 0), V tiles (warp 2), each
-      // item's query tiles and cos/sin rows (warp 3) ----------------
+      // ---------------- producers: K tiles (warp 0), V tiles (one half each
+      // from warps 2 and 3), each item's query tiles and cos/sin rows (warp 3,
+      // before that item's V halves) ----------------
       if (lane == 0) {
         const bool is_k = warp == 0, is_q = warp == 3;
+        // each V tile's two 64-dimension halves come from warps 2 and 3
+        // (the bulk-tensor engine's rate is per issuing warp)
+        const bool vhalf = warp >= 2;
         const CUtensorMap* map = is_k ? &kmap : &vmap;
         const uint32_t full = is_k ? k_full : v_full, empty = is_k ? k_empty : v_empty;
         const uint32_t ring = sb + (is_k ? kKOff : kVOff);
@@ -213,9 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&cmap);
             prefetch_tensormap(&smap);
           }
-        } else {
-          prefetch_tensormap(map);
         }
+        prefetch_tensormap(map);
         bool waited = false;  // griddepcontrol.wait, before the first K/V copy
         int g = 0;            // tiles issued into this ring, over the CTA's items
         int kq = 0;           // items whose query tiles were issued
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pf::tma_load_5d(sb + kQOff, &qmap, 0, w.i0, 0, w.h0, w.b, q_full);
             ++kq;
           }
-          if (is_q) continue;
+
           if (!waited) {
             pdl_wait_primary();  // the new K/V rows are the append kernel's
             waited = true;
@@ -269,10 +275,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full + 8 * st, kTileBytes);
-            // both 64-dimension halves in one box: the map's third dimension
-            // steps to the row's second half
-            pf::tma_load_4d(ring + st * kTileBytes, map, 0, j * kBN, 0, zkv, full + 8 * st);
+            if (vhalf) {
+              mbar_arrive_expect_tx(full + 8 * st, kKVBox);
+              pf::tma_load_4d(ring + st * kTileBytes + (warp - 2) * kKVBox, map, 0, j * kBN, warp - 2, zkv,
+                              full + 8 * st);
+            } else {
+              // both 64-dimension halves in one box: the map's third
+              // dimension steps to the row's second half
+              mbar_arrive_expect_tx(full + 8 * st, kTileBytes);
+              pf::tma_load_4d(ring + st * kTileBytes, map, 0, j * kBN, 0, zkv, full + 8 * st);
+            }
           }
         }
         // no copy may still be in flight into shared memory when the CTA exits
@@ -280,8 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(q_full, (kq - 1) & 1, p.err);
           mbar_wait(cs_full, (kq - 1) & 1, p.err);
         }
-        if (!is_q)
-          for (int t = max(0, g - kSt); t < g; ++t) mbar_wait(full + 8 * (t % kSt), (t / kSt) & 1, p.err);
+        for (int t = max(0, g - kSt); t < g; ++t) mbar_wait(full + 8 * (t % kSt), (t / kSt) & 1, p.err);
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -646,8 +657,9 @@ cudaError_t launch_t(const ForwardArgs& a, const void* q_src) {
     const cuuint64_t dims[4] = {64, (cuuint64_t)a.M, 2, (cuuint64_t)a.B * a.Hkv};
     const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, 128, (cuuint64_t)a.M * kD * 2};
     const cuuint32_t box[4] = {64, (cuuint32_t)kBN, 2, 1};
+    const cuuint32_t hbox[4] = {64, (cuuint32_t)kBN, 1, 1};  // V: one half per producer warp
     if (!encode_tensor_map(&kmap, dt, 4, a.kbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map(&vmap, dt, 4, a.vbuf, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+        !encode_tensor_map(&vmap, dt, 4, a.vbuf, dims, strides, hbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   if (a.cos) {
