@@ -402,7 +402,8 @@ def cpu_baseline(name, min_seconds=10.0):
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
     "decode_b16": 111111680 + 3026944,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
-    "chunked_prefill": 65953280 + 6172416,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
+    "prefill_2k": 111838464 + 31110144,    # prefill_dual_kernel, profiles/prefill_dual_kernel_prefill_2k.md
+    "chunked_prefill": 65992960 + 6409728,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
 }
 # the attention kernel of each prefill workload: two query heads per CTA
 # where the group size is even and there is no bias or window
