@@ -79,13 +79,13 @@ __device__ __forceinline__ void rotate_vec(const T* src, T* dst, const T* cosr, 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(128) rope_append_kernel(RopeParams p) {
   using V = VecT<T, VEC>;
-  // the attention kernel after this one (programmatic dependent launch)
-  // may start its own prologue; it waits for this grid before it reads the
-  // buffer.  This grid is itself launched that way: its CTAs may be resident
-  // before the kernel ahead of it (any kernel) has completed, and read
-  // nothing until it has.
-  pdl_launch_dependents();
+  // This grid is launched as a programmatic dependent of the kernel ahead of
+  // it (any kernel): its CTAs may be resident before that kernel has
+  // completed, and read nothing until it has.  Only then may the attention
+  // kernel after this one start its prologue, which reads the call's inputs
+  // (query rows, cos/sin rows, seqlens_k) before it waits for this grid.
   pdl_wait_primary();
+  pdl_launch_dependents();
   if (p.sched.base && blockIdx.x == 0) {
     psched::build(p.sched, p.sched_cap);
     return;
