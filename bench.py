@@ -491,7 +491,7 @@ def run_ours(args):
             wo = W.CONFIGS[other]
             kvo = 2 * wo.batch * wo.kv_num_heads * wo.max_seq_len * wo.head_size * 2
             p2 = Problem(other, device, sets=4 if kvo < (1 << 30) else 1)
-            steps = 20 if not p2.decode else 50
+            steps = 50
             # ~0.5 s of load first, so that the clock samples cover this workload
             tb2 = time.time()
             k = 0
