@@ -85,7 +85,7 @@ constexpr int kExactTiles = GQA_DECODE_EXACT_TILES;  // ... and the first chunk'
 #define GQA_DECODE_SHORT_TILES 24
 #endif
 constexpr int kShortTilesPerCta = GQA_DECODE_SHORT_TILES;  // see chunk_target
-constexpr int kMergeBatch = 4;               // partials loaded per round of a merge (registers)
+constexpr int kMergeBatch = 5;               // partials loaded per round of a merge (registers)
 
 // Descriptor of one chunk, written by the producer into a staging slot.
 struct ChunkDesc {
