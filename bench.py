@@ -401,7 +401,7 @@ def cpu_baseline(name, min_seconds=10.0):
 # kernel per launch, from the ncu captures summarised in profiles/; a kernel
 # changed since its capture has no entry (reported as null).
 TRAFFIC = {
-    "decode_b16": 111111680 + 3026944,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
+    "decode_b16": 111568384 + 3243264,     # decode_dyn_kernel, profiles/decode_dyn_kernel_decode_b16.md
     "prefill_2k": 111838464 + 31110144,    # prefill_dual_kernel, profiles/prefill_dual_kernel_prefill_2k.md
     "chunked_prefill": 65992960 + 6409728,  # prefill_head_kernel, profiles/prefill_head_kernel_chunked_prefill.md
 }
