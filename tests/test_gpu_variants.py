@@ -33,6 +33,9 @@ def _lib():
     dict(S=150, past=(0, 40, 300), M=512, interleaved=1, dtype="fp16", seed=304),  # prefill, interleaved
     dict(S=5, D=64, past=(3, 0, 40), M=64, seed=305),                 # generic kernel
     dict(S=4, D=128, rotary=False, past=(0, 4, 8), M=32, seed=306),   # prefill without rotary
+    # a grid of 640 one-head items (the two-head prefill kernel on 152 SMs),
+    # G = 20, ragged pasts, interleaved rotary
+    dict(S=128, B=4, H=160, Hkv=8, past=(0, 50, 130, 7), M=512, interleaved=1, seed=307),
 ])
 def test_packed_qkv_matches_oracle(kw):
     inp = custom(**kw)
